@@ -1,0 +1,177 @@
+"""Seeded synthetic inputs for the GEMM and transpose workloads.
+
+This module is shared by the tests, the benchmark and the smoke check; it
+holds no arithmetic of the contraction itself, only sampling and the
+rounding of sampled float32 values into the stored formats (bfloat16,
+FP8 E4M3FN, E8M0 scale bytes).  It imports neither the CUDA binding nor the
+oracle.
+
+Every workload draws from ``numpy.random.default_rng(seed)``; the recipes:
+
+=====  ========================================================================
+name   recipe
+=====  ========================================================================
+tiny   M=N=128, K=256; A, B ~ U[-1, 1) -> bf16; fp32 D            (seed 1)
+sq4k   M=N=K=4096; A, B ~ N(0, 1) -> bf16; bf16 D                 (seed 2)
+sq8k   M=N=K=8192; A, B ~ N(0, 1)/sqrt(8192) -> bf16; fp32 D      (seed 3)
+mx8k   M=N=K=8192; A, B = E4M3(clamp(N(0, 1), +-448)); SFA, SFB bytes
+       127 + U{-4..4} (scale 2^U{-4..4}) per 32 K elements; bf16 D (seed 4)
+ragged M=4000, N=3000, K=1000; A, B ~ U[-1, 1) -> bf16; D = A B^T + 1,
+       fp32 D                                                      (seed 5)
+tr8k   8192 x 8192 random 16-bit patterns (NaN patterns included)  (seed 6)
+=====  ========================================================================
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Rounding sampled float32 values into the stored formats
+# ---------------------------------------------------------------------------
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (round to nearest, ties to even); uint16 bits.
+
+    Inputs are finite samples; NaN/Inf handling is not needed here.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    return ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bfloat16 bit patterns to float32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_e4m3fn_bits(x: np.ndarray) -> np.ndarray:
+    """Round to FP8 E4M3FN (nearest, ties to even), saturating at +-448; uint8 bits.
+
+    Normal numbers: value = (1 + f/8) * 2^(e-7), e in 1..15 (e=15,f=7 is NaN);
+    subnormals: value = f/8 * 2^-6.
+    """
+    v = np.clip(np.asarray(x, dtype=np.float64), -448.0, 448.0)
+    sign = (v < 0) | ((v == 0) & np.signbit(v))
+    a = np.abs(v)
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    # Subnormal range: quantum 2^-9; a result of 8 quanta is the smallest
+    # normal, whose code (exponent field 1, fraction 0) is also 8.
+    code[sub] = np.rint(a[sub] / 2.0 ** -9).astype(np.int64)
+    nrm = ~sub
+    mant, expo = np.frexp(a[nrm])          # a = mant * 2^expo, mant in [0.5, 1)
+    e = expo - 1                           # a = (2*mant) * 2^e, 2*mant in [1, 2)
+    q = np.rint((2.0 * mant - 1.0) * 8.0).astype(np.int64)
+    carry = q == 8
+    e = e + carry
+    q = np.where(carry, 0, q)
+    code[nrm] = ((e + 7) << 3) | q
+    return (code | (sign.astype(np.int64) << 7)).astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# Samplers
+# ---------------------------------------------------------------------------
+
+def bf16_uniform(rng: np.random.Generator, shape, lo=-1.0, hi=1.0) -> np.ndarray:
+    return f32_to_bf16_bits(rng.uniform(lo, hi, size=shape).astype(np.float32))
+
+
+def bf16_normal(rng: np.random.Generator, shape, scale=1.0) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if scale != 1.0:
+        x *= np.float32(scale)
+    return f32_to_bf16_bits(x)
+
+
+def bf16_quarter_integers(rng: np.random.Generator, shape) -> np.ndarray:
+    """randint(-4, 5) / 4, exact in bf16 (the data of the tcgen05.mma example)."""
+    return f32_to_bf16_bits((rng.integers(-4, 5, size=shape) / 4).astype(np.float32))
+
+
+def e4m3_normal(rng: np.random.Generator, shape) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    return f32_to_e4m3fn_bits(x)
+
+
+def e8m0_scales(rng: np.random.Generator, shape, lo=-4, hi=4) -> np.ndarray:
+    """E8M0 bytes 127 + U{lo..hi}, i.e. scales 2^U{lo..hi}."""
+    return (127 + rng.integers(lo, hi + 1, size=shape)).astype(np.uint8)
+
+
+def b16_bits(rng: np.random.Generator, shape) -> np.ndarray:
+    return rng.integers(0, 1 << 16, size=shape, dtype=np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Workloads
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str          # "bf16", "mxfp8" or "transpose"
+    M: int
+    N: int
+    K: int
+    seed: int
+    d_dtype: str       # "f32" or "bf16" (GEMM output)
+    epi_add: float     # epilogue constant (0: plain product)
+    cta_pair: bool     # launch with cta_group::2 pairs
+    describe: str
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K if self.kind != "transpose" else 0
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", "bf16", 128, 128, 256, 1, "f32", 0.0, False,
+                     "bf16 GEMM 128x128x256, U[-1,1) inputs, fp32 D"),
+    "sq4k": Workload("sq4k", "bf16", 4096, 4096, 4096, 2, "bf16", 0.0, False,
+                     "bf16 GEMM 4096^3, N(0,1) inputs, bf16 D, 128x256 tiles"),
+    "sq8k": Workload("sq8k", "bf16", 8192, 8192, 8192, 3, "f32", 0.0, True,
+                     "bf16 GEMM 8192^3, N(0,1)/sqrt(K) inputs, fp32 D, CTA pairs"),
+    "mx8k": Workload("mx8k", "mxfp8", 8192, 8192, 8192, 4, "bf16", 0.0, True,
+                     "MXFP8 GEMM 8192^3, E4M3 x E8M0/32 inputs, bf16 D"),
+    "ragged": Workload("ragged", "bf16", 4000, 3000, 1000, 5, "f32", 1.0, False,
+                       "bf16 GEMM 4000x3000x1000 + 1, U[-1,1) inputs, fp32 D"),
+    "tr8k": Workload("tr8k", "transpose", 8192, 8192, 0, 6, "b16", 0.0, False,
+                     "b16 transpose 8192x8192, random bit patterns"),
+}
+
+
+def make_inputs(w: Workload | str, M: int | None = None, N: int | None = None,
+                K: int | None = None, seed: int | None = None) -> dict:
+    """Host (numpy) inputs of a workload; sizes/seed may be overridden.
+
+    bf16:      {"A": uint16 [M,K], "B": uint16 [N,K]}
+    mxfp8:     {"A": uint8 [M,K], "B": uint8 [N,K], "SFA": uint8 [M,K/32],
+                "SFB": uint8 [N,K/32]}
+    transpose: {"X": uint16 [M,N]}
+    """
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    M = w.M if M is None else M
+    N = w.N if N is None else N
+    K = w.K if K is None else K
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    if w.kind == "transpose":
+        return {"X": b16_bits(rng, (M, N))}
+    if w.kind == "mxfp8":
+        return {
+            "A": e4m3_normal(rng, (M, K)),
+            "B": e4m3_normal(rng, (N, K)),
+            "SFA": e8m0_scales(rng, (M, K // 32)),
+            "SFB": e8m0_scales(rng, (N, K // 32)),
+        }
+    if w.name in ("tiny", "ragged"):
+        return {"A": bf16_uniform(rng, (M, K)), "B": bf16_uniform(rng, (N, K))}
+    if w.name == "sq8k":
+        s = 1.0 / math.sqrt(K)
+        return {"A": bf16_normal(rng, (M, K), s), "B": bf16_normal(rng, (N, K), s)}
+    return {"A": bf16_normal(rng, (M, K)), "B": bf16_normal(rng, (N, K))}
