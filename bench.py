@@ -1,0 +1,451 @@
+"""Benchmark of the tiled-contraction hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input
+(inputs resident in HBM):
+  * gemm_bf16              8192^3, bf16 in, f32 D, CTA pairs (cta_group::2)
+  * gemm_mxfp8_blockscaled 8192^3, E4M3 x E8M0/32 in, bf16 D, CTA pairs
+                           (its scale-image rearrangement kernel included)
+  * tile_transpose_b16     8192 x 8192 16-bit patterns
+value = GEMM FLOPs of the step (2*M*N*K for each GEMM) / device time of the
+step, in TFLOP/s.  The inputs of one step (516 MB) exceed the 129 MB L2 and
+every kernel's operands are evicted by the other kernels' traffic before
+they are used again, so no separate L2 flush is inserted.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (float64, the machine's host cores) on
+a bounded sample of the same workload per step and prints the same JSON
+line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from blackwell_tile_gemm_gb300 import synth  # noqa: E402
+
+METRIC = "GEMM TFLOP/s at 1 GB300 (bf16, MXFP8) and % of dense tensor-pipe peak"
+UNIT = "TFLOP/s"
+SIZE = 8192
+WORKLOAD = ("bf16 GEMM 8192^3 fp32 D (CTA pairs) + MXFP8 GEMM 8192^3 bf16 D (CTA pairs) "
+            "+ b16 transpose 8192^2")
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=5)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def make_step_inputs(torch, dev):
+    def bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def u8(bits):
+        return torch.from_numpy(bits).to(dev)
+
+    host = {
+        "bf16": synth.make_inputs("sq8k"),
+        "mx": synth.make_inputs("mx8k"),
+        "tr": synth.make_inputs("tr8k"),
+    }
+    d = {
+        "A": bf16(host["bf16"]["A"]), "B": bf16(host["bf16"]["B"]),
+        "mA": u8(host["mx"]["A"]), "mB": u8(host["mx"]["B"]),
+        "SFA": u8(host["mx"]["SFA"]), "SFB": u8(host["mx"]["SFB"]),
+        "X": torch.from_numpy(host["tr"]["X"].view(np.int16)).to(dev),
+        "D": torch.empty((SIZE, SIZE), dtype=torch.float32, device=dev),
+        "mD": torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=dev),
+        "XT": torch.empty((SIZE, SIZE), dtype=torch.int16, device=dev),
+    }
+    return host, d
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import blackwell_tile_gemm_gb300 as tg
+    from blackwell_tile_gemm_gb300 import build as tgbuild
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    tgbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    host, d = make_step_inputs(torch, dev)
+    flops_gemm = 2 * SIZE ** 3
+    flops_step = 2 * flops_gemm
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tg.gemm_bf16(d["A"], d["B"], d["D"], cta_pair=True, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        tg.gemm_mxfp8_blockscaled(d["mA"], d["mB"], d["SFA"], d["SFB"], d["mD"], cta_pair=True,
+                                  stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        tg.tile_transpose_b16(d["X"], d["XT"], stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, site = tg.tg_device_status()
+    if code != tg.TG_OK:
+        raise SystemExit(f"device status {code} (site {site}) during warm-up")
+
+    barrier(world)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    code, site = tg.tg_device_status()
+    if code != tg.TG_OK:
+        raise SystemExit(f"device status {code} (site {site}) in the timed region")
+    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                    for e in evs])
+    total_ms = reduce_max(total_ms, world)
+    ms_step = total_ms / args.steps
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    bf16_ms, mx_ms, tr_ms = (float(per[:, i].mean()) for i in range(3))
+    peak_bf16 = float(peaks["bf16_tflops"])
+    kern = {
+        "gemm_bf16": {"ms": bf16_ms, "tflops": flops_gemm / (bf16_ms * 1e-3) / 1e12},
+        "gemm_mxfp8_blockscaled": {"ms": mx_ms, "tflops": flops_gemm / (mx_ms * 1e-3) / 1e12},
+        "tile_transpose_b16": {"ms": tr_ms, "gbs": 2 * 2 * SIZE * SIZE / (tr_ms * 1e-3) / 1e9},
+    }
+    kern["gemm_bf16"]["frac_of_bf16_peak"] = kern["gemm_bf16"]["tflops"] / peak_bf16
+    kern["gemm_mxfp8_blockscaled"]["frac_of_2x_bf16_peak"] = (
+        kern["gemm_mxfp8_blockscaled"]["tflops"] / (2 * peak_bf16))
+    kern["tile_transpose_b16"]["frac_of_hbm_peak"] = (
+        kern["tile_transpose_b16"]["gbs"] / float(peaks["hbm_gbs"]))
+    dominant = max(("gemm_bf16", "gemm_mxfp8_blockscaled"), key=lambda n: kern[n]["ms"])
+    if dominant == "gemm_bf16":
+        achieved, peak = kern["gemm_bf16"]["tflops"], peak_bf16
+        peak_note = f"bf16 cuBLAS burst, {peak_src}"
+    else:
+        achieved, peak = kern[dominant]["tflops"], 2 * peak_bf16
+        peak_note = f"2 x bf16 cuBLAS burst (fp8/bf16 nominal ratio), {peak_src}"
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": peak_note}
+
+    e2e = measure_e2e(torch, tg, host, dev, stream, args.e2e_steps, flops_step)
+    cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1 and args.cpu_seconds > 0) \
+        else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3 (f32 accumulate)",
+        "data": "synthetic (seeded numpy; recipes in blackwell_tile_gemm_gb300/synth.py)",
+        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
+                   "tiles": "256x256 per CTA pair, 128-byte K stages",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "not flushed: 516 MB of step inputs > 129 MB L2"},
+        "roofline": roofline, "kernels": kern, "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(torch, tg, host, dev, stream, steps, flops_step):
+    """Same step through the public API with pinned host buffers: H2D of the
+    step's inputs, the three calls, D2H of the three results, every step."""
+    if steps <= 0:
+        return None
+    pin = {}
+    for k, arr in (("A", host["bf16"]["A"]), ("B", host["bf16"]["B"]),
+                   ("mA", host["mx"]["A"]), ("mB", host["mx"]["B"]),
+                   ("SFA", host["mx"]["SFA"]), ("SFB", host["mx"]["SFB"]),
+                   ("X", host["tr"]["X"])):
+        t = torch.from_numpy(arr.view(np.int16) if arr.dtype == np.uint16 else arr)
+        pin[k] = t.pin_memory()
+    out_h = {
+        "D": torch.empty((SIZE, SIZE), dtype=torch.float32).pin_memory(),
+        "mD": torch.empty((SIZE, SIZE), dtype=torch.int16).pin_memory(),
+        "XT": torch.empty((SIZE, SIZE), dtype=torch.int16).pin_memory(),
+    }
+    devb = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pin.items()}
+    D = torch.empty((SIZE, SIZE), dtype=torch.float32, device=dev)
+    mD = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=dev)
+    XT = torch.empty((SIZE, SIZE), dtype=torch.int16, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_h.values())
+
+    def one():
+        for k in pin:
+            devb[k].copy_(pin[k], non_blocking=True)
+        tg.gemm_bf16(devb["A"].view(torch.bfloat16), devb["B"].view(torch.bfloat16), D,
+                     cta_pair=True, stream=stream)
+        tg.gemm_mxfp8_blockscaled(devb["mA"], devb["mB"], devb["SFA"], devb["SFB"], mD,
+                                  cta_pair=True, stream=stream)
+        tg.tile_transpose_b16(devb["X"], XT, stream=stream)
+        out_h["D"].copy_(D, non_blocking=True)
+        out_h["mD"].copy_(mD.view(torch.int16), non_blocking=True)
+        out_h["XT"].copy_(XT, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": flops_step / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+_SAMPLE = {}
+
+
+def _oracle_sample_inputs():
+    if not _SAMPLE:
+        _SAMPLE["bf16"] = synth.make_inputs("sq8k")
+        _SAMPLE["mx"] = synth.make_inputs("mx8k")
+    return _SAMPLE
+
+
+def oracle_sample(rows_per_gemm: int, cols: int, offset: int):
+    """Oracle on `rows_per_gemm` full-K rows x `cols` columns of each 8192^3
+    GEMM; returns (flops, seconds)."""
+    import oracle
+    x = _oracle_sample_inputs()
+    rows = (np.arange(rows_per_gemm) * 61 + offset) % SIZE
+    cs = (np.arange(cols) * 37 + offset) % SIZE
+    t0 = time.perf_counter()
+    oracle.gemm_bf16(x["bf16"]["A"], x["bf16"]["B"], rows=rows, cols=cs)
+    oracle.gemm_mxfp8(x["mx"]["A"], x["mx"]["B"], x["mx"]["SFA"], x["mx"]["SFB"],
+                      rows=rows, cols=cs)
+    dt = time.perf_counter() - t0
+    return 2 * 2 * rows_per_gemm * cols * SIZE, dt
+
+
+def cpu_baseline(target_seconds: float):
+    import oracle
+    oracle.build()
+    _oracle_sample_inputs()
+    cores = oracle.num_threads()
+    rows = max(cores, 16)
+    flops, dt = oracle_sample(rows, 1024, 0)            # calibration
+    scale = max(1.0, target_seconds / max(dt, 1e-3))
+    rows = int(rows * scale)
+    flops, dt = oracle_sample(rows, 1024, 1)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "seconds": dt,
+            "sample": (f"float64 oracle on {rows} rows x 1024 columns (all K = 8192) of each "
+                       f"8192^3 GEMM (bf16 and MXFP8), operands decoded per call")}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    _oracle_sample_inputs()
+    cores = oracle.num_threads()
+    rows, cols = cores, 256
+    for _ in range(args.warmup):
+        oracle_sample(rows, cols, 0)
+    flops = 0.0
+    secs = 0.0
+    for k in range(args.steps):
+        f, dt = oracle_sample(rows, cols, k + 1)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    sample = (f"per step: float64 oracle on {rows} rows x {cols} columns (all K = 8192) of "
+              f"each 8192^3 GEMM (bf16 and MXFP8)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy; recipes in blackwell_tile_gemm_gb300/synth.py)",
+        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
+                   "parallelism": "host cores (OpenMP over output rows)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (one process per GPU; replicas, no data exchange)
+# ---------------------------------------------------------------------------
+
+_PG = {"init": False}
+
+
+def init_dist(world, local):
+    if world <= 1:
+        return
+    import torch
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    _PG["init"] = True
+
+
+def barrier(world):
+    if world > 1 and _PG["init"]:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world <= 1 or not _PG["init"]:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    init_dist(world, local)
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if _PG["init"]:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+"""GB300-native tiled GEMM (D = A @ B.T) -- Python binding of libtgemm.so.
+
+The binding only marshals arguments: it passes device pointers, row strides,
+sizes and the current CUDA stream to the C entry points declared in
+``include/tgemm.h``; every step of the computation runs in the library's
+CUDA kernels.  PyTorch provides device memory and streams.  There is no
+fallback: if the library is not built, the first call raises.
+
+Entry points (same names as the C ABI):
+
+* ``gemm_bf16(A, B, D=None, ...)``                -- bf16 x bf16 -> f32 / bf16
+* ``gemm_mxfp8_blockscaled(A, B, SFA, SFB, ...)`` -- E4M3 x E8M0/32 -> f32 / bf16
+* ``tile_transpose_b16(X, out=None)``             -- 16-bit transpose, bit-exact
+* ``tg_device_status(stream=None)``               -- device-side error record
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libtgemm.so")
+
+TG_OK = 0
+TG_ERR_INVALID_ARG = 1
+TG_ERR_MISALIGNED = 2
+TG_ERR_UNSUPPORTED = 3
+TG_ERR_CUDA = 4
+TG_ERR_TIMEOUT = 5
+TG_D_F32 = 0
+TG_D_BF16 = 1
+TG_EPI_NONE = 0
+TG_EPI_ADD_SCALAR = 1
+TG_FLAG_CTA_PAIR = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TgError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = status_string(code) if _lib is not None else str(code)
+        detail = ""
+        if code == TG_ERR_CUDA and _lib is not None:
+            detail = f" (cudaError {_lib.tg_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}{detail} [status {code}]")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtgemm.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m blackwell_tile_gemm_gb300.build` "
+                "(the package has no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
+        L.gemm_bf16.restype = i32
+        L.gemm_bf16.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, i32,
+                                ctypes.c_float, u32, vp]
+        L.gemm_mxfp8_blockscaled.restype = i32
+        L.gemm_mxfp8_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                             i64, i64, i64, i32, i32, ctypes.c_float, u32, vp]
+        L.tile_transpose_b16.restype = i32
+        L.tile_transpose_b16.argtypes = [vp, i64, vp, i64, i64, i64, vp]
+        L.tg_device_status.restype = i32
+        L.tg_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.tg_set_wait_timeout_ns.restype = i32
+        L.tg_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        L.tg_status_string.restype = ctypes.c_char_p
+        L.tg_status_string.argtypes = [i32]
+        L.tg_last_cuda_error.restype = i32
+        L.tg_last_cuda_error.argtypes = []
+        L.tg_version.restype = i32
+        L.tg_version.argtypes = []
+        _lib = L
+        return L
+
+
+def status_string(code: int) -> str:
+    return lib().tg_status_string(int(code)).decode()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != TG_OK:
+        raise TgError(rc, what)
+
+
+def _rows(t, name):
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[0] > 0 and t.shape[1] > 0 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit inner stride")
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def _ld(t, name, mult):
+    """Row stride in elements; a single-row tensor may report any stride."""
+    ld = _rows(t, name)
+    if t.shape[0] <= 1:
+        ld = -(-max(t.shape[1], 1) // mult) * mult
+    return ld
+
+
+def _d_code(dtype):
+    import torch
+    if dtype == torch.float32:
+        return TG_D_F32
+    if dtype == torch.bfloat16:
+        return TG_D_BF16
+    raise ValueError(f"D must be float32 or bfloat16, got {dtype}")
+
+
+def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, cta_pair=False, stream=None):
+    """D[M,N] = A[M,K] @ B[N,K].T (+ epilogue_add), bf16 inputs, f32 accumulation.
+
+    A, B: CUDA bfloat16 tensors with unit inner stride.  D: optional output
+    (float32 or bfloat16, [M, N]); otherwise allocated with ``out_dtype``
+    (default float32).  ``cta_pair`` selects the two-CTA (cta_group::2) kernel.
+    """
+    import torch
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A is [M, K] and B is [N, K]")
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("gemm_bf16 takes bfloat16 A and B")
+    if D is None:
+        D = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    if tuple(D.shape) != (M, N):
+        raise ValueError("D must be [M, N]")
+    epi = TG_EPI_NONE if epilogue_add is None else TG_EPI_ADD_SCALAR
+    rc = lib().gemm_bf16(A.data_ptr(), _ld(A, "A", 8), B.data_ptr(), _ld(B, "B", 8),
+                         D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
+                         float(epilogue_add or 0.0), TG_FLAG_CTA_PAIR if cta_pair else 0,
+                         _stream_handle(stream))
+    _check(rc, "gemm_bf16")
+    return D
+
+
+def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_add=None,
+                           cta_pair=False, stream=None):
+    """Block-scaled MXFP8 product: D = (A * 2^(SFA-127)) @ (B * 2^(SFB-127)).T.
+
+    A: [M, K], B: [N, K] E4M3FN bytes (torch.float8_e4m3fn or uint8); SFA:
+    [M, K/32], SFB: [N, K/32] E8M0 bytes (uint8).  D float32 or bfloat16
+    (default bfloat16).
+    """
+    import torch
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A is [M, K] and B is [N, K]")
+    for name, t in (("A", A), ("B", B), ("SFA", SFA), ("SFB", SFB)):
+        if t.element_size() != 1:
+            raise TypeError(f"{name} must hold 1-byte elements")
+    if tuple(SFA.shape) != (M, K // 32) or tuple(SFB.shape) != (N, K // 32):
+        raise ValueError("SFA must be [M, K/32] and SFB [N, K/32]")
+    if D is None:
+        D = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=A.device)
+    if tuple(D.shape) != (M, N):
+        raise ValueError("D must be [M, N]")
+    epi = TG_EPI_NONE if epilogue_add is None else TG_EPI_ADD_SCALAR
+    rc = lib().gemm_mxfp8_blockscaled(
+        A.data_ptr(), _ld(A, "A", 16), B.data_ptr(), _ld(B, "B", 16),
+        SFA.data_ptr(), _ld(SFA, "SFA", 1), SFB.data_ptr(), _ld(SFB, "SFB", 1),
+        D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
+        float(epilogue_add or 0.0), TG_FLAG_CTA_PAIR if cta_pair else 0, _stream_handle(stream))
+    _check(rc, "gemm_mxfp8_blockscaled")
+    return D
+
+
+def tile_transpose_b16(X, out=None, *, stream=None):
+    """out[j, i] = X[i, j] for any 16-bit dtype (bits moved unchanged)."""
+    import torch
+    rows, cols = X.shape
+    if X.element_size() != 2:
+        raise TypeError("tile_transpose_b16 moves 16-bit elements")
+    if out is None:
+        out = torch.empty((cols, rows), dtype=X.dtype, device=X.device)
+    if tuple(out.shape) != (cols, rows) or out.element_size() != 2:
+        raise ValueError("out must be [cols, rows] of a 16-bit dtype")
+    rc = lib().tile_transpose_b16(X.data_ptr(), _ld(X, "X", 8), out.data_ptr(),
+                                  _ld(out, "out", 8), rows, cols, _stream_handle(stream))
+    _check(rc, "tile_transpose_b16")
+    return out
+
+
+def tg_device_status(stream=None):
+    """Synchronise the stream; return (status, site) and clear the record."""
+    site = ctypes.c_uint32(0)
+    rc = lib().tg_device_status(_stream_handle(stream), ctypes.byref(site))
+    return int(rc), int(site.value)
+
+
+def tg_set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().tg_set_wait_timeout_ns(int(ns)), "tg_set_wait_timeout_ns")

@@ -1,0 +1,280 @@
+// C entry points of libtgemm.so: argument checks, per-device state, the
+// device status record, tensor-map encoding and the MXFP8 workspace.
+//
+// Every check happens before any launch, following the pages' rule that a
+// contract violation is rejected rather than repaired ("Explicit CUDA tile
+// patterns", section "Group, repeat, and atom axes": a failed contract is an
+// error, never a search for another layout; "cp.async.bulk.tensor", section
+// "Legality conditions": 16-byte aligned bases and outer byte strides).
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/tgemm.h"
+#include "tg_internal.h"
+
+namespace tg {
+
+// Status record of each device: [0] code, [1] wait site, [2] block, [3] thread.
+__device__ uint32_t g_status_record[4];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceCtx g_ctx[kMaxDevices];
+uint64_t g_timeout_ns = 2000000000ull;
+thread_local int t_last_cuda_error = 0;
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+Workspace g_workspace[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return TG_ERR_CUDA;
+}
+
+uint64_t wait_timeout_ns() {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  return g_timeout_ns;
+}
+
+DeviceCtx* current_ctx() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    cuda_fail(cudaErrorInvalidDevice);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mutex);
+  DeviceCtx& c = g_ctx[dev];
+  if (c.device == dev) return &c;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return nullptr;
+  }
+  void* st = nullptr;
+  e = cudaGetSymbolAddress(&st, g_status_record);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return nullptr;
+  }
+  c.num_sms = sms;
+  c.status = static_cast<uint32_t*>(st);
+  c.device = dev;
+  return &c;
+}
+
+int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                       uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                       uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      cudaError_t e =
+          cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return cuda_fail(cudaErrorSymbolNotFound);
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  // A zero extent is not encodable; callers never launch for empty problems,
+  // but keep a valid map (extent 1) for unused descriptor parameters.
+  if (inner == 0) inner = 1;
+  if (outer == 0) outer = 1;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return TG_OK;
+}
+
+void* device_workspace(size_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  Workspace& w = g_workspace[dev];
+  if (w.bytes >= bytes && w.ptr) return w.ptr;
+  if (w.ptr) {
+    // Earlier work on any stream may still read the old buffer.
+    if (cudaDeviceSynchronize() != cudaSuccess) return nullptr;
+    cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, want);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return nullptr;
+  }
+  w.ptr = p;
+  w.bytes = want;
+  return p;
+}
+
+int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
+                const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D,
+                int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
+                float epi_scalar, unsigned flags, cudaStream_t stream, DeviceCtx* ctx) {
+  const int epi_add = epilogue == TG_EPI_ADD_SCALAR ? 1 : 0;
+  if (K == 0)
+    return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi_add ? epi_scalar : 0.0f, stream);
+  const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
+  if (!mx)
+    return launch_gemm_bf16_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M),
+                                 static_cast<int>(N), static_cast<int>(K), d_dtype, epi_add,
+                                 epi_scalar, pair, stream, ctx);
+  uint8_t* ws = static_cast<uint8_t*>(device_workspace(mxfp8_workspace_bytes(M, N, K, pair)));
+  if (ws == nullptr) return TG_ERR_CUDA;
+  return launch_gemm_mxfp8_impl(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
+                                static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                                d_dtype, epi_add, epi_scalar, pair, ws, stream, ctx);
+}
+
+}  // namespace tg
+
+using namespace tg;
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+
+int check_gemm_common(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
+                      int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
+                      unsigned flags, int a_esize) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return TG_ERR_INVALID_ARG;
+  if (d_dtype != TG_D_F32 && d_dtype != TG_D_BF16) return TG_ERR_INVALID_ARG;
+  if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_ADD_SCALAR) return TG_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR)) return TG_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return TG_OK;
+  if (D == nullptr || ldd < N) return TG_ERR_INVALID_ARG;
+  const int d_esize = d_dtype == TG_D_F32 ? 4 : 2;
+  if (!aligned16(D) || (ldd * d_esize) % 16 != 0) return TG_ERR_MISALIGNED;
+  if (K == 0) return TG_OK;
+  if (A == nullptr || B == nullptr || lda < K || ldb < K) return TG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B)) return TG_ERR_MISALIGNED;
+  if ((lda * a_esize) % 16 != 0 || (ldb * a_esize) % 16 != 0) return TG_ERR_MISALIGNED;
+  return TG_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+              int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue, float epi_scalar,
+              unsigned flags, void* cuda_stream) {
+  int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 2);
+  if (rc != TG_OK || M == 0 || N == 0) return rc;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  return launch_gemm(false, A, lda, B, ldb, nullptr, 0, nullptr, 0, D, ldd, M, N, K, d_dtype,
+                     epilogue, epi_scalar, flags, as_stream(cuda_stream), ctx);
+}
+
+int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           int epilogue, float epi_scalar, unsigned flags, void* cuda_stream) {
+  if (K % 32 != 0) return TG_ERR_INVALID_ARG;
+  int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 1);
+  if (rc != TG_OK || M == 0 || N == 0) return rc;
+  if (K > 0) {
+    if (SFA == nullptr || SFB == nullptr || ld_sfa < K / 32 || ld_sfb < K / 32)
+      return TG_ERR_INVALID_ARG;
+  }
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  return launch_gemm(true, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K, d_dtype,
+                     epilogue, epi_scalar, flags, as_stream(cuda_stream), ctx);
+}
+
+int tile_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out, int64_t rows,
+                       int64_t cols, void* cuda_stream) {
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return TG_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return TG_OK;
+  if (in == nullptr || out == nullptr || ld_in < cols || ld_out < rows) return TG_ERR_INVALID_ARG;
+  if (!aligned16(in) || !aligned16(out) || ld_in % 8 != 0 || ld_out % 8 != 0)
+    return TG_ERR_MISALIGNED;
+  // in spans [in, in + 2*((rows-1)*ld_in + cols)), out likewise: reject overlap.
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(in);
+  const uintptr_t a1 = a0 + 2u * static_cast<uintptr_t>((rows - 1) * ld_in + cols);
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t b1 = b0 + 2u * static_cast<uintptr_t>((cols - 1) * ld_out + rows);
+  if (a0 < b1 && b0 < a1) return TG_ERR_INVALID_ARG;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  return launch_transpose_b16(in, ld_in, out, ld_out, rows, cols, as_stream(cuda_stream), ctx);
+}
+
+int tg_device_status(void* cuda_stream, uint32_t* site) {
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(as_stream(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  uint32_t rec[4] = {0, 0, 0, 0};
+  e = cudaMemcpyFromSymbol(rec, g_status_record, sizeof(rec));
+  if (e != cudaSuccess) return cuda_fail(e);
+  const uint32_t zero[4] = {0, 0, 0, 0};
+  e = cudaMemcpyToSymbol(g_status_record, zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (site) *site = rec[1];
+  return static_cast<int>(rec[0]);
+}
+
+int tg_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return TG_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  g_timeout_ns = ns;
+  return TG_OK;
+}
+
+const char* tg_status_string(int status) {
+  switch (status) {
+    case TG_OK: return "ok";
+    case TG_ERR_INVALID_ARG: return "invalid argument";
+    case TG_ERR_MISALIGNED: return "misaligned pointer or row stride";
+    case TG_ERR_UNSUPPORTED: return "unsupported request";
+    case TG_ERR_CUDA: return "CUDA error";
+    case TG_ERR_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int tg_last_cuda_error(void) { return t_last_cuda_error; }
+
+int tg_version(void) { return 100; }
+
+}  // extern "C"

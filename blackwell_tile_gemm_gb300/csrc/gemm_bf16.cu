@@ -1,0 +1,84 @@
+// Dense bf16 GEMM configurations (kind::f16, f32 accumulation).
+//
+//   single CTA : 128 x 256 tiles, 4-stage ring of 48 KB, two 256-column
+//                accumulators in tensor memory (all 512 columns).
+//   CTA pair   : 256 x 256 tiles per cluster of two (cta_group::2), each CTA
+//                stages 128 rows of A and 128 rows of B per stage (32 KB),
+//                6-stage ring, two accumulators per CTA.
+#include "gemm_launch.cuh"
+
+namespace tg {
+
+namespace {
+using CfgF32 = GemmCfg<1, false, 256, 2, 4, false>;
+using CfgBf16 = GemmCfg<1, false, 256, 2, 4, true>;
+using CfgPairF32 = GemmCfg<2, false, 256, 2, 6, false>;
+using CfgPairBf16 = GemmCfg<2, false, 256, 2, 6, true>;
+}  // namespace
+
+int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
+                          int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
+                          float epi_scalar, bool pair, cudaStream_t stream, DeviceCtx* ctx) {
+  constexpr int BN = 256;
+  const int g = pair ? 2 : 1;
+  const int b_rows = BN / g;
+  CUtensorMap tA, tB;
+  int rc = make_tensor_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, lda * 2, 64, 128,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != TG_OK) return rc;
+  rc = make_tensor_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, ldb * 2, 64, b_rows,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != TG_OK) return rc;
+  GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.num_m_tiles = ceil_div_i(M, 128 * g);
+  a.num_n_tiles = ceil_div_i(N, BN);
+  a.num_k_blocks = ceil_div_i(K, 64);
+  a.D = D;
+  a.ldd = ldd;
+  a.epi_scalar = epi_scalar;
+  a.epi_add = epi_add;
+  a.status = ctx->status;
+  a.timeout_ns = wait_timeout_ns();
+  const bool bf16_out = d_dtype == TG_D_BF16;
+  if (!pair)
+    return bf16_out ? launch_gemm_cfg<CfgBf16>(tA, tB, tA, tB, a, stream, ctx)
+                    : launch_gemm_cfg<CfgF32>(tA, tB, tA, tB, a, stream, ctx);
+  return bf16_out ? launch_gemm_cfg<CfgPairBf16>(tA, tB, tA, tB, a, stream, ctx)
+                  : launch_gemm_cfg<CfgPairF32>(tA, tB, tA, tB, a, stream, ctx);
+}
+
+// ---------------------------------------------------------------------------
+// K == 0: D = epilogue(0)
+// ---------------------------------------------------------------------------
+
+namespace {
+__global__ void fill_kernel(void* D, int64_t ldd, int64_t M, int64_t N, int bf16_out,
+                            float value) {
+  const int64_t total = M * N;
+  const uint16_t vb = static_cast<uint16_t>(pack_bf16x2(value, value) & 0xFFFFu);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N, c = i % N;
+    if (bf16_out)
+      reinterpret_cast<uint16_t*>(D)[r * ldd + c] = vb;
+    else
+      reinterpret_cast<float*>(D)[r * ldd + c] = value;
+  }
+}
+}  // namespace
+
+int launch_fill_epilogue(void* D, int64_t ldd, int64_t M, int64_t N, int d_dtype, float value,
+                         cudaStream_t stream) {
+  const int64_t total = M * N;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(D, ldd, M, N,
+                                                                 d_dtype == TG_D_BF16, value);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TG_OK : cuda_fail(e);
+}
+
+}  // namespace tg

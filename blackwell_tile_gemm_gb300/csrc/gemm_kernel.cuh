@@ -1,0 +1,426 @@
+// Persistent, warp-specialised tcgen05 GEMM: D[M,N] = A[M,K] * B[N,K]^T.
+//
+// The operation and its operand roles follow "tcgen05.mma" (TVM TIRx tile
+// operation guide), sections "Operands and repeat axes" (per-CTA canonical
+// shapes D (M/g, N), A (M/g, K), B (N/g, K); SFB carries the full N in each
+// CTA of a pair), "Shared descriptors are byte-stride contracts" (K-major,
+// 128-byte swizzled rows, next 8-row group at SDO) and "Examples" (explicit K
+// decomposition into K16 issues, one commit per issue sequence, tcgen05.ld
+// 32x32b read-back).  TMA staging follows "cp.async.bulk.tensor" (one elected
+// thread, mbarrier with expected transaction bytes, out-of-range boxes read
+// zeros).  The pages leave pipelining, election and scheduling to the caller;
+// this file is that caller code:
+//
+//   warp 0      TMA producer: one lane waits for a free ring slot, posts the
+//               expected bytes and issues the A / B (and scale-image) loads.
+//   warp 1      TMEM allocator and MMA issuer: one lane waits for a full slot,
+//               (copies the scale images into TMEM,) issues the K16 / K32
+//               MMAs, and commits to the slot's "empty" barrier; at the end of
+//               a tile it commits to the accumulator's "full" barrier.
+//   warps 2..5  epilogue: wait for a full accumulator, tcgen05.ld 32 columns
+//               at a time (row = TMEM lane), apply the scalar op, convert and
+//               store with st.global.v4; release the accumulator.
+//
+// Tiles are visited persistently (one CTA or CTA pair per SM, static stride)
+// in grouped order so that CTAs running at the same time share A and B panels
+// in L2.  Every wait is bounded (see tg_ptx.cuh: mbar_wait).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "tg_ptx.cuh"
+
+namespace tg {
+
+enum : uint32_t {
+  kSiteProducerEmpty = 1,
+  kSiteMmaFull = 2,
+  kSiteMmaAccEmpty = 3,
+  kSiteEpiAccFull = 4,
+};
+
+struct GemmArgs {
+  int M, N, K;
+  int num_m_tiles;  // tiles of kCtaGroup*128 rows
+  int num_n_tiles;  // tiles of BN columns
+  int num_k_blocks; // stages of BK elements
+  void* D;
+  int64_t ldd;
+  float epi_scalar;
+  int epi_add;      // 0: D = acc; 1: D = acc + epi_scalar
+  int sfa_blocks;   // 128-row blocks per K group in the SFA image
+  int sfb_blocks;   // 128-row blocks per K group in the SFB image
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+template <int kCtaGroup_, bool kMx_, int kBN_, int kAccBufs_, int kStages_, bool kBf16Out_>
+struct GemmCfg {
+  static constexpr int kCtaGroup = kCtaGroup_;
+  static constexpr bool kMx = kMx_;
+  static constexpr int BM = 128;                    // D rows per CTA (TMEM lanes)
+  static constexpr int BN = kBN_;                   // D columns per tile (MMA N)
+  static constexpr int kAccBufs = kAccBufs_;
+  static constexpr int kStages = kStages_;
+  static constexpr bool kBf16Out = kBf16Out_;
+  static constexpr int BK = kMx ? 128 : 64;         // K elements per stage = 128 bytes
+  static constexpr int UMMA_K = kMx ? 32 : 16;      // K elements per MMA issue = 32 bytes
+  static constexpr int kIssues = BK / UMMA_K;       // 4 issues per stage
+  static constexpr int B_ROWS = BN / kCtaGroup;     // B rows this CTA stages
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = B_ROWS * 128;
+  static constexpr int SFA_BYTES = kMx ? 512 : 0;   // 128 rows x 4 K-blocks
+  static constexpr int SFB_BYTES = kMx ? (BN / 128) * 512 : 0;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  // shared memory carve-up (offsets from a 1024-aligned base)
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + kStages * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + kStages * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + kStages * SFA_BYTES;
+  static constexpr int OFF_BAR = (OFF_SFB + kStages * SFB_BYTES + 7) & ~7;
+  static constexpr int NUM_BARS = 2 * kStages + 2 * kAccBufs + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  // tensor memory columns
+  static constexpr int ACC_COLS = BN;
+  static constexpr int SFA_COLS = kMx ? 4 : 0;
+  static constexpr int SFB_COLS = kMx ? BN / 32 : 0;
+  static constexpr int SF_COL0 = ACC_COLS * kAccBufs;
+  static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int TMEM_USED = SF_COL0 + SF_STAGE_COLS * kStages;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                   : TMEM_USED <= 64  ? 64
+                                   : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256
+                                                      : 512;
+  static constexpr uint32_t MMA_M = BM * kCtaGroup;
+  static constexpr int kThreads = 192;
+  static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
+};
+
+// Grouped tile order: consecutive tile ids walk down a band of kGroup m-tiles
+// before moving to the next n-tile.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& tm, int& tn) {
+  constexpr int kGroup = 16;
+  const int per_group = kGroup * num_n;
+  const int g = t / per_group;
+  const int first_m = g * kGroup;
+  const int gm = min(num_m - first_m, kGroup);
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+template <class C>
+__device__ __forceinline__ void epilogue_store_chunk(const GemmArgs& p, int row, int col0,
+                                                     const uint32_t (&v)[32]) {
+  const float add = p.epi_add ? p.epi_scalar : 0.0f;
+  if constexpr (C::kBf16Out) {
+    uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + static_cast<int64_t>(row) * p.ldd;
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) + add, __uint_as_float(v[2 * i + 1]) + add);
+    if (col0 + 32 <= p.N) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        st_global_v4(drow + col0 + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = col0 + 8 * i;
+        if (c + 8 <= p.N) {
+          st_global_v4(drow + c, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (c + e < p.N)
+              drow[c + e] = static_cast<uint16_t>(w[4 * i + e / 2] >> (16 * (e & 1)));
+        }
+      }
+    }
+  } else {
+    float* drow = reinterpret_cast<float*>(p.D) + static_cast<int64_t>(row) * p.ldd;
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(v[i]) + add);
+    if (col0 + 32 <= p.N) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        st_global_v4(drow + col0 + 4 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = col0 + 4 * i;
+        if (c + 4 <= p.N) {
+          st_global_v4(drow + c, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (c + e < p.N) drow[c + e] = __uint_as_float(w[4 * i + e]);
+        }
+      }
+    }
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSFA,
+                        const __grid_constant__ CUtensorMap tmSFB, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full_bar = bars;                          // [kStages]  TMA -> MMA
+  uint64_t* empty_bar = bars + C::kStages;            // [kStages]  MMA -> TMA
+  uint64_t* accf_bar = bars + 2 * C::kStages;         // [kAccBufs] MMA -> epilogue
+  uint64_t* acce_bar = accf_bar + C::kAccBufs;        // [kAccBufs] epilogue -> MMA
+  uint64_t* drain_bar = acce_bar + C::kAccBufs;       // MMA completion on give-up
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t rank = (C::kCtaGroup == 2) ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 4 * C::kCtaGroup);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    if constexpr (C::kMx) {
+      prefetch_tensormap(&tmSFA);
+      prefetch_tensormap(&tmSFB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc<C::kCtaGroup>(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish<C::kCtaGroup>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (C::kCtaGroup == 2) cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitGuard guard{p.status, abort_flag, p.timeout_ns};
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int unit = blockIdx.x / C::kCtaGroup;         // CTA or CTA pair index
+  const int num_units = gridDim.x / C::kCtaGroup;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_ab = policy_evict_last();
+      const uint32_t sA = smem_addr(smem + C::OFF_A);
+      const uint32_t sB = smem_addr(smem + C::OFF_B);
+      const uint32_t sSFA = smem_addr(smem + C::OFF_SFA);
+      const uint32_t sSFB = smem_addr(smem + C::OFF_SFB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;   // per-stage bit masks
+      bool ok = true;
+      for (int t = unit; t < num_tiles && ok; t += num_units) {
+        int tm, tn;
+        tile_coords(t, p.num_m_tiles, p.num_n_tiles, tm, tn);
+        const int a_row = tm * C::MMA_M + static_cast<int>(rank) * C::BM;
+        const int b_row = tn * C::BN + static_cast<int>(rank) * C::B_ROWS;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, guard, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const int kx = kb * C::BK;
+          if constexpr (C::kCtaGroup == 1) {
+            const uint32_t fb = smem_addr(&full_bar[stage]);
+            mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_TX);
+            tma_load_2d(sA + stage * C::A_BYTES, &tmA, fb, kx, a_row, pol_ab);
+            tma_load_2d(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+            if constexpr (C::kMx) {
+              tma_load_2d(sSFA + stage * C::SFA_BYTES, &tmSFA, fb, 0, kb * p.sfa_blocks + tm,
+                          pol_ab);
+              tma_load_2d(sSFB + stage * C::SFB_BYTES, &tmSFB, fb, 0,
+                          kb * p.sfb_blocks + tn * (C::BN / 128), pol_ab);
+            }
+          } else {
+            // Both CTAs' loads complete on the leader's barrier; only the
+            // leader posts the expected byte count (for the pair).
+            const uint32_t fb = map_to_cta(smem_addr(&full_bar[stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_TX);
+            tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, fb, kx, a_row, pol_ab);
+            tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+            if constexpr (C::kMx) {
+              tma_load_2d_pair(sSFA + stage * C::SFA_BYTES, &tmSFA, fb, 0,
+                               kb * p.sfa_blocks + tm * 2 + static_cast<int>(rank), pol_ab);
+              tma_load_2d_pair(sSFB + stage * C::SFB_BYTES, &tmSFB, fb, 0,
+                               kb * p.sfb_blocks + tn * (C::BN / 128), pol_ab);
+            }
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // Gave up: let the loads already issued land before the CTA exits.
+        for (int s = 0; s < C::kStages; ++s)
+          if (issued & (1u << s))
+            mbar_wait_drain(&full_bar[s], (issued_parity >> s) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      const uint32_t sA = smem_addr(smem + C::OFF_A);
+      const uint32_t sB = smem_addr(smem + C::OFF_B);
+      const uint32_t sSFA = smem_addr(smem + C::OFF_SFA);
+      const uint32_t sSFB = smem_addr(smem + C::OFF_SFB);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = unit; t < num_tiles && ok; t += num_units) {
+        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, guard, kSiteMmaAccEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, guard, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = sA + stage * C::A_BYTES;
+          const uint32_t b0 = sB + stage * C::B_BYTES;
+          if constexpr (C::kMx) {
+            const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_STAGE_COLS;
+            const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+            // 32 rows x 16 bytes per copy; rows 8 apart by 128 bytes.
+            tmem_cp_32x128b_warpx4<C::kCtaGroup>(
+                sfa_t, make_smem_desc(sSFA + stage * C::SFA_BYTES, 16, 128, kDescSwizzleNone));
+#pragma unroll
+            for (int j = 0; j < C::BN / 128; ++j)
+              tmem_cp_32x128b_warpx4<C::kCtaGroup>(
+                  sfb_t + 4 * j,
+                  make_smem_desc(sSFB + stage * C::SFB_BYTES + 512 * j, 16, 128,
+                                 kDescSwizzleNone));
+#pragma unroll
+            for (int k = 0; k < C::kIssues; ++k) {
+              const uint64_t ad = make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B);
+              const uint64_t bd = make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B);
+              mma_mxf8<C::kCtaGroup>(d_tmem, ad, bd, idesc_mxf8_e4m3(C::MMA_M, C::BN, k, k),
+                                     sfa_t, sfb_t, (kb | k) != 0);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < C::kIssues; ++k) {
+              const uint64_t ad = make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B);
+              const uint64_t bd = make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B);
+              mma_bf16<C::kCtaGroup>(d_tmem, ad, bd, idesc_bf16_f32(C::MMA_M, C::BN),
+                                     (kb | k) != 0);
+            }
+          }
+          if constexpr (C::kCtaGroup == 1)
+            mma_commit(&empty_bar[stage]);
+          else
+            mma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if constexpr (C::kCtaGroup == 1)
+          mma_commit(&accf_bar[acc]);
+        else
+          mma_commit_pair(&accf_bar[acc], 0x3);
+        if (++acc == C::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok || *abort_flag) {
+        // Gave up: wait until every MMA issued so far has finished with
+        // shared and tensor memory before they are released.
+        if constexpr (C::kCtaGroup == 1)
+          mma_commit(drain_bar);
+        else
+          mma_commit_pair(drain_bar, 0x1);
+        mbar_wait_drain(drain_bar, 0, p.timeout_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int slab = warp & 3;                        // TMEM lanes 32*slab .. +31
+    const int row_in_tile = slab * 32 + static_cast<int>(lane);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t acce_remote = 0;
+    if constexpr (C::kCtaGroup == 2) acce_remote = map_to_cta(smem_addr(&acce_bar[0]), 0);
+    for (int t = unit; t < num_tiles; t += num_units) {
+      int tm, tn;
+      tile_coords(t, p.num_m_tiles, p.num_n_tiles, tm, tn);
+      if (!mbar_wait(&accf_bar[acc], acc_phase, guard, kSiteEpiAccFull)) break;
+      tc_fence_after_sync();
+      const int row = tm * C::MMA_M + static_cast<int>(rank) * C::BM + row_in_tile;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(slab * 32) << 16) +
+                             static_cast<uint32_t>(acc * C::ACC_COLS);
+#pragma unroll 1
+      for (int c = 0; c < C::BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + 32 * c, v);
+        tmem_ld_wait();
+        const int col0 = tn * C::BN + 32 * c;
+        if (row < p.M && col0 < p.N) epilogue_store_chunk<C>(p, row, col0, v);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (C::kCtaGroup == 1)
+          mbar_arrive(&acce_bar[acc]);
+        else
+          mbar_arrive_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+      }
+      if (++acc == C::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (C::kCtaGroup == 2) cluster_sync();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc<C::kCtaGroup>(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace tg

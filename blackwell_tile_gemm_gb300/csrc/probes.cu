@@ -1,0 +1,350 @@
+// Probe kernels: the pages' worked examples and raw mapping dumps, one CTA
+// each.  Declared in include/tgemm_probes.h.
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/tgemm_probes.h"
+#include "tg_internal.h"
+#include "tg_ptx.cuh"
+
+namespace tg {
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int launched() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TG_OK : cuda_fail(e);
+}
+
+// --------------------------------------------------------------- add one (v4)
+__global__ void add_one_kernel(const float* a, float* b) {
+  const int t = threadIdx.x;   // (warp, lane) flattened; 12 words per thread
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int off = (t * 3 + r) * 4;
+    const uint4 v = ld_global_v4(a + off);
+    st_global_v4(b + off, __float_as_uint(__uint_as_float(v.x) + 1.0f),
+                 __float_as_uint(__uint_as_float(v.y) + 1.0f),
+                 __float_as_uint(__uint_as_float(v.z) + 1.0f),
+                 __float_as_uint(__uint_as_float(v.w) + 1.0f));
+  }
+}
+
+// ------------------------------------------------- ldmatrix interleaved example
+__global__ void ldmatrix_x2_interleaved_kernel(const uint32_t* x, uint32_t* out) {
+  __shared__ __align__(16) uint32_t SM[256];   // (16, 4, 2) : (8, 1, 128) words
+  const int lane = threadIdx.x;
+  for (int q = 0; q < 4; ++q) {
+    const int n = lane + 32 * q;
+    SM[8 * (n / 8) + (n / 2) % 4 + 128 * (n % 2)] = x[n];
+  }
+  __syncthreads();
+  uint32_t raw[12];
+#pragma unroll
+  for (int i = 0; i < 12; ++i) raw[i] = 4294966519u;
+  const int m = (lane >> 3) & 1, r = lane & 7;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    // row (k, m, r) of the view is SM[2r+m, 0.., k]: word 8*(2r+m) + 128k
+    const uint32_t addr = smem_addr(&SM[8 * (2 * r + m) + 128 * k]);
+    ldmatrix_x2(addr, raw[8 * k + 0], raw[8 * k + 2]);
+  }
+#pragma unroll
+  for (int i = 0; i < 12; ++i) out[lane * 12 + i] = raw[i];
+}
+
+// ------------------------------------------------------ ldmatrix / stmatrix dumps
+template <int N, bool kTrans>
+__global__ void ldmatrix_dump_kernel(const uint16_t* img, uint32_t* out) {
+  __shared__ __align__(16) uint16_t sm[4 * 64];
+  const int lane = threadIdx.x;
+  for (int i = lane; i < N * 64; i += 32) sm[i] = img[i];
+  __syncthreads();
+  const int mat = (lane >> 3) % N, row = lane & 7;
+  const uint32_t addr = smem_addr(&sm[(mat * 8 + row) * 8]);
+  uint32_t r[4] = {0, 0, 0, 0};
+  if constexpr (N == 1) {
+    if constexpr (kTrans) ldmatrix_x1_trans(addr, r[0]); else ldmatrix_x1(addr, r[0]);
+  } else if constexpr (N == 2) {
+    if constexpr (kTrans) ldmatrix_x2_trans(addr, r[0], r[1]); else ldmatrix_x2(addr, r[0], r[1]);
+  } else {
+    if constexpr (kTrans) ldmatrix_x4_trans(addr, r[0], r[1], r[2], r[3]);
+    else ldmatrix_x4(addr, r[0], r[1], r[2], r[3]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) out[lane * N + i] = r[i];
+}
+
+template <int N, bool kTrans>
+__global__ void stmatrix_dump_kernel(const uint32_t* regs, uint16_t* out) {
+  __shared__ __align__(16) uint16_t sm[4 * 64];
+  const int lane = threadIdx.x;
+  for (int i = lane; i < 4 * 64; i += 32) sm[i] = 0;
+  __syncthreads();
+  uint32_t r[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < N; ++i) r[i] = regs[lane * N + i];
+  const int mat = (lane >> 3) % N, row = lane & 7;
+  const uint32_t addr = smem_addr(&sm[(mat * 8 + row) * 8]);
+  if constexpr (N == 1) {
+    if constexpr (kTrans) stmatrix_x1_trans(addr, r[0]); else stmatrix_x1(addr, r[0]);
+  } else if constexpr (N == 2) {
+    if constexpr (kTrans) stmatrix_x2_trans(addr, r[0], r[1]); else stmatrix_x2(addr, r[0], r[1]);
+  } else {
+    if constexpr (kTrans) stmatrix_x4_trans(addr, r[0], r[1], r[2], r[3]);
+    else stmatrix_x4(addr, r[0], r[1], r[2], r[3]);
+  }
+  __syncthreads();
+  for (int i = lane; i < N * 64; i += 32) out[i] = sm[i];
+}
+
+// ------------------------------------------------------------- TMA two boxes
+__global__ void tma_two_boxes_kernel(const __grid_constant__ CUtensorMap map, uint32_t* out,
+                                     uint32_t* status, uint64_t timeout_ns) {
+  __shared__ __align__(128) uint32_t sh[2 * 8 * 16];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x;
+  if (lane == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_arrive_expect_tx(&bar, 1024);
+  }
+  __syncthreads();
+  if (lane == 0) {
+    const uint64_t pol = policy_evict_first();
+    for (int g = 0; g < 2; ++g)   // coords (row, col) = (8g, 0); PTX order is (col, row)
+      tma_load_2d(smem_addr(&sh[g * 128]), &map, smem_addr(&bar), 0, 8 * g, pol);
+  }
+  const WaitGuard guard{status, &abort_flag, timeout_ns};
+  const bool ok = mbar_wait(&bar, 0, guard, 90);
+  __syncthreads();
+  if (ok)
+    for (int g = 0; g < 2; ++g)
+      for (int r = 0; r < 8; ++r)
+        if (lane < 16) out[(g * 8 + r) * 16 + lane] = sh[g * 128 + r * 16 + lane];
+}
+
+// ------------------------------------------------------- TMA 128B swizzle dump
+__global__ void tma_swizzle_kernel(const __grid_constant__ CUtensorMap map, int rows,
+                                   uint8_t* out, uint32_t* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t dyn[];
+  uint8_t* img = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(rows) * 128u);
+    tma_load_2d(smem_addr(img), &map, smem_addr(&bar), 0, 0, policy_evict_first());
+  }
+  __syncthreads();
+  const WaitGuard guard{status, &abort_flag, timeout_ns};
+  const bool ok = mbar_wait(&bar, 0, guard, 91);
+  __syncthreads();
+  if (ok)
+    for (int i = t; i < rows * 128; i += blockDim.x) out[i] = img[i];
+}
+
+// ---------------------------------------------------- tcgen05 128x64x64 example
+__global__ void __launch_bounds__(128) mma_128x64x64_kernel(const uint16_t* a, const uint16_t* b,
+                                                            float* out, uint32_t* status,
+                                                            uint64_t timeout_ns) {
+  extern __shared__ uint8_t dyn[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sa = base;               // 128 rows x 128 B, 128B-swizzled, K-major
+  uint8_t* sb = base + 128 * 128;   // 64 rows x 128 B
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == 0) tmem_alloc<1>(&tmem_slot, 64);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  // Ordinary stores into the swizzled K-major image: 16-byte chunk c of row r
+  // goes to chunk c ^ (r % 8) of that row.
+  for (int c = 0; c < 8; ++c) {
+    const uint4 v = ld_global_v4(a + tid * 64 + c * 8);
+    *reinterpret_cast<uint4*>(sa + tid * 128 + ((c ^ (tid & 7)) << 4)) = v;
+    if (tid < 64) {
+      const uint4 w = ld_global_v4(b + tid * 64 + c * 8);
+      *reinterpret_cast<uint4*>(sb + tid * 128 + ((c ^ (tid & 7)) << 4)) = w;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (tid == 0) {
+    const uint32_t a0 = smem_addr(sa), b0 = smem_addr(sb);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mma_bf16<1>(tmem, make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B),
+                  make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B),
+                  idesc_bf16_f32(128, 64), k != 0);
+    mma_commit(&bar);
+  }
+  __syncwarp();
+  const WaitGuard guard{status, &abort_flag, timeout_ns};
+  const bool ok = mbar_wait(&bar, 0, guard, 92);
+  tc_fence_after_sync();
+  if (ok) {
+    const int row = warp * 32 + lane;
+    for (int c = 0; c < 2; ++c) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) out[row * 64 + 32 * c + j] = __uint_as_float(v[j]);
+    }
+  } else if (tid == 0) {
+    mbar_wait_drain(&bar, 0, timeout_ns);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc<1>(tmem, 64);
+  }
+}
+
+// --------------------------------------------------------------- wait timeout
+__global__ void wait_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);          // nothing ever arrives
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitGuard guard{status, &abort_flag, timeout_ns};
+    mbar_wait(&bar, 0, guard, 99);
+  }
+}
+
+}  // namespace
+}  // namespace tg
+
+using namespace tg;
+
+extern "C" {
+
+int tg_probe_add_one_v4(const float* a, float* b, void* s) {
+  if (!a || !b) return TG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b)) return TG_ERR_MISALIGNED;
+  add_one_kernel<<<1, 64, 0, static_cast<cudaStream_t>(s)>>>(a, b);
+  return launched();
+}
+
+int tg_probe_ldmatrix_x2_interleaved(const uint32_t* x, uint32_t* out, void* s) {
+  if (!x || !out) return TG_ERR_INVALID_ARG;
+  ldmatrix_x2_interleaved_kernel<<<1, 32, 0, static_cast<cudaStream_t>(s)>>>(x, out);
+  return launched();
+}
+
+int tg_probe_ldmatrix(const uint16_t* img, int n, int trans, uint32_t* out, void* s) {
+  if (!img || !out || (n != 1 && n != 2 && n != 4) || (trans != 0 && trans != 1))
+    return TG_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  if (n == 1) {
+    if (trans) ldmatrix_dump_kernel<1, true><<<1, 32, 0, st>>>(img, out);
+    else ldmatrix_dump_kernel<1, false><<<1, 32, 0, st>>>(img, out);
+  } else if (n == 2) {
+    if (trans) ldmatrix_dump_kernel<2, true><<<1, 32, 0, st>>>(img, out);
+    else ldmatrix_dump_kernel<2, false><<<1, 32, 0, st>>>(img, out);
+  } else {
+    if (trans) ldmatrix_dump_kernel<4, true><<<1, 32, 0, st>>>(img, out);
+    else ldmatrix_dump_kernel<4, false><<<1, 32, 0, st>>>(img, out);
+  }
+  return launched();
+}
+
+int tg_probe_stmatrix(const uint32_t* regs, int n, int trans, uint16_t* out, void* s) {
+  if (!regs || !out || (n != 1 && n != 2 && n != 4) || (trans != 0 && trans != 1))
+    return TG_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  if (n == 1) {
+    if (trans) stmatrix_dump_kernel<1, true><<<1, 32, 0, st>>>(regs, out);
+    else stmatrix_dump_kernel<1, false><<<1, 32, 0, st>>>(regs, out);
+  } else if (n == 2) {
+    if (trans) stmatrix_dump_kernel<2, true><<<1, 32, 0, st>>>(regs, out);
+    else stmatrix_dump_kernel<2, false><<<1, 32, 0, st>>>(regs, out);
+  } else {
+    if (trans) stmatrix_dump_kernel<4, true><<<1, 32, 0, st>>>(regs, out);
+    else stmatrix_dump_kernel<4, false><<<1, 32, 0, st>>>(regs, out);
+  }
+  return launched();
+}
+
+int tg_probe_tma_two_boxes(const uint32_t* a, uint32_t* out, void* s) {
+  if (!a || !out) return TG_ERR_INVALID_ARG;
+  if (!aligned16(a)) return TG_ERR_MISALIGNED;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  CUtensorMap map;
+  int rc = make_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, a, 16, 16, 64, 16, 8,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != TG_OK) return rc;
+  tma_two_boxes_kernel<<<1, 32, 0, static_cast<cudaStream_t>(s)>>>(map, out, ctx->status,
+                                                                   wait_timeout_ns());
+  return launched();
+}
+
+int tg_probe_tma_swizzle128(const uint16_t* src, int rows, uint8_t* out, void* s) {
+  if (!src || !out || rows < 8 || rows > 256 || rows % 8 != 0) return TG_ERR_INVALID_ARG;
+  if (!aligned16(src)) return TG_ERR_MISALIGNED;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  CUtensorMap map;
+  int rc = make_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, 64,
+                              static_cast<uint64_t>(rows), 128, 64, static_cast<uint32_t>(rows),
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != TG_OK) return rc;
+  const int smem = rows * 128 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(tma_swizzle_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 33 * 1024);
+  if (e != cudaSuccess) return cuda_fail(e);
+  tma_swizzle_kernel<<<1, 128, smem, static_cast<cudaStream_t>(s)>>>(map, rows, out, ctx->status,
+                                                                     wait_timeout_ns());
+  return launched();
+}
+
+int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, void* s) {
+  if (!a || !b || !out) return TG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b)) return TG_ERR_MISALIGNED;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  const int smem = 128 * 128 + 64 * 128 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mma_128x64x64_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  mma_128x64x64_kernel<<<1, 128, smem, static_cast<cudaStream_t>(s)>>>(a, b, out, ctx->status,
+                                                                       wait_timeout_ns());
+  return launched();
+}
+
+int tg_probe_wait_timeout(uint64_t timeout_ns, void* s) {
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull) return TG_ERR_INVALID_ARG;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(s)>>>(ctx->status, timeout_ns);
+  return launched();
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Host-side pieces shared by the translation units of libtgemm.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/tgemm.h"
+
+namespace tg {
+
+// Per-device state, created on first use of a device.
+struct DeviceCtx {
+  int device = -1;
+  int num_sms = 0;
+  uint32_t* status = nullptr;      // device address of the 4-word status record
+};
+
+// Context of the current device (cudaGetDevice); nullptr on CUDA failure
+// (the failure is recorded for tg_last_cuda_error).
+DeviceCtx* current_ctx();
+
+// Records a CUDA error for tg_last_cuda_error() and returns TG_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+
+// Deadline of bounded device waits (ns).
+uint64_t wait_timeout_ns();
+
+// 2-D tiled tensor map over a row-major array: `inner` elements per row
+// (contiguous), `outer` rows, `row_bytes` between rows.  Box = box_inner x
+// box_outer elements.  Out-of-range box elements read zeros.
+int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                       uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                       uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+// Library-owned device workspace for the current device, at least `bytes`
+// long (grown on demand).  nullptr on failure.
+void* device_workspace(size_t bytes);
+
+// Launchers (arguments already validated).
+int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
+                const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D,
+                int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
+                float epi_scalar, unsigned flags, cudaStream_t stream, DeviceCtx* ctx);
+
+int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
+                          int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
+                          float epi_scalar, bool pair, cudaStream_t stream, DeviceCtx* ctx);
+
+int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
+                           float epi_scalar, bool pair, uint8_t* sf_workspace,
+                           cudaStream_t stream, DeviceCtx* ctx);
+
+// Bytes of scale-image workspace the MXFP8 path needs for this problem.
+size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair);
+
+// D = epilogue(0) when K == 0.
+int launch_fill_epilogue(void* D, int64_t ldd, int64_t M, int64_t N, int d_dtype, float value,
+                         cudaStream_t stream);
+
+int launch_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out, int64_t rows,
+                         int64_t cols, cudaStream_t stream, DeviceCtx* ctx);
+
+}  // namespace tg

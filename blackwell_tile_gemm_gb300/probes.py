@@ -1,0 +1,75 @@
+"""Python binding of the probe kernels declared in include/tgemm_probes.h.
+
+Each probe runs one of the pages' worked examples, or dumps one hardware
+mapping, in a single CTA; the tests compare the results with the oracle.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _check, _stream_handle, lib
+
+_ready = False
+
+
+def _L():
+    global _ready
+    L = lib()
+    if not _ready:
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        for name, args in {
+            "tg_probe_add_one_v4": [vp, vp, vp],
+            "tg_probe_ldmatrix_x2_interleaved": [vp, vp, vp],
+            "tg_probe_ldmatrix": [vp, i32, i32, vp, vp],
+            "tg_probe_stmatrix": [vp, i32, i32, vp, vp],
+            "tg_probe_tma_two_boxes": [vp, vp, vp],
+            "tg_probe_tma_swizzle128": [vp, i32, vp, vp],
+            "tg_probe_mma_128x64x64": [vp, vp, vp, vp],
+            "tg_probe_wait_timeout": [ctypes.c_uint64, vp],
+        }.items():
+            f = getattr(L, name)
+            f.restype = i32
+            f.argtypes = args
+        _ready = True
+    return L
+
+
+def add_one_v4(a, b, stream=None):
+    _check(_L().tg_probe_add_one_v4(a.data_ptr(), b.data_ptr(), _stream_handle(stream)),
+           "tg_probe_add_one_v4")
+
+
+def ldmatrix_x2_interleaved(x, out, stream=None):
+    _check(_L().tg_probe_ldmatrix_x2_interleaved(x.data_ptr(), out.data_ptr(),
+                                                 _stream_handle(stream)),
+           "tg_probe_ldmatrix_x2_interleaved")
+
+
+def ldmatrix(img, n, trans, out, stream=None):
+    _check(_L().tg_probe_ldmatrix(img.data_ptr(), int(n), int(trans), out.data_ptr(),
+                                  _stream_handle(stream)), "tg_probe_ldmatrix")
+
+
+def stmatrix(regs, n, trans, out, stream=None):
+    _check(_L().tg_probe_stmatrix(regs.data_ptr(), int(n), int(trans), out.data_ptr(),
+                                  _stream_handle(stream)), "tg_probe_stmatrix")
+
+
+def tma_two_boxes(a, out, stream=None):
+    _check(_L().tg_probe_tma_two_boxes(a.data_ptr(), out.data_ptr(), _stream_handle(stream)),
+           "tg_probe_tma_two_boxes")
+
+
+def tma_swizzle128(src, rows, out, stream=None):
+    _check(_L().tg_probe_tma_swizzle128(src.data_ptr(), int(rows), out.data_ptr(),
+                                        _stream_handle(stream)), "tg_probe_tma_swizzle128")
+
+
+def mma_128x64x64(a, b, out, stream=None):
+    _check(_L().tg_probe_mma_128x64x64(a.data_ptr(), b.data_ptr(), out.data_ptr(),
+                                       _stream_handle(stream)), "tg_probe_mma_128x64x64")
+
+
+def wait_timeout(timeout_ns, stream=None):
+    _check(_L().tg_probe_wait_timeout(int(timeout_ns), _stream_handle(stream)),
+           "tg_probe_wait_timeout")

@@ -1,0 +1,148 @@
+/*
+ * tgemm -- tiled dense contraction D = A * B^T on GB300 (sm_103a).
+ *
+ * C ABI of libtgemm.so.  Every entry point takes plain pointers, sizes and a
+ * CUDA stream handle; no C++ or PyTorch type crosses this boundary.
+ *
+ * Sources for the operations (TVM TIRx documentation pages):
+ *   [MMA]  "tcgen05.mma", section "Examples" -- B is stored as (N, K) and the
+ *          result is a @ b.T; section "Weight-stationary and block scaling"
+ *          for .block_scale with SFA/SFB.
+ *   [TMA]  "cp.async.bulk.tensor", sections "Operand specification" and
+ *          "Legality conditions" -- 16-byte aligned global bases, unit inner
+ *          stride and suitably aligned outer byte strides; out-of-range box
+ *          elements read the fill value (oob_fill 0 = zero).
+ *   [LDM]  "ldmatrix / stmatrix", section "Transpose and stores" -- .trans
+ *          transposes each 8x8 matrix of 16-bit elements.
+ *   [EW]   "Explicit CUDA tile patterns", section "Scalar compositions", and
+ *          "Tile Operands and Execution" -- an elementwise scalar function
+ *          applied to each register element before the store.
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller allocates and owns every buffer.  The library
+ *     allocates no device memory for bf16 GEMM or the transpose; the MXFP8
+ *     call keeps one library-owned scale-image workspace per device (grown
+ *     on demand, never shrunk, freed at process exit).
+ *   - Strides are in ELEMENTS and describe row-major 2-D arrays (unit inner
+ *     stride).  Pointers are device pointers and must be 16-byte aligned;
+ *     every row stride times the element size must be a multiple of 16 bytes.
+ *   - Execution is asynchronous on `cuda_stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  A host-detectable error returns a non-zero
+ *     tg_status BEFORE anything is launched.  Errors the device detects (a
+ *     pipeline wait that exceeded its deadline) are reported by
+ *     tg_device_status().  Nothing is thrown across the boundary and there
+ *     is no CPU fallback: an unsupported request returns TG_ERR_UNSUPPORTED.
+ *   - Calls on one stream are ordered; calls on different streams that share
+ *     an output race, as with any CUDA kernel.
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARG = 1, /* null pointer, negative size, stride < row length */
+  TG_ERR_MISALIGNED = 2,  /* pointer or row stride violates the 16-byte rule  */
+  TG_ERR_UNSUPPORTED = 3, /* valid request outside what is implemented         */
+  TG_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                 */
+  TG_ERR_TIMEOUT = 5      /* (device) a pipeline wait passed its deadline      */
+} tg_status;
+
+/* Element type of D. */
+enum { TG_D_F32 = 0, TG_D_BF16 = 1 };
+
+/* Fused elementwise epilogue, applied to the f32 accumulator before the
+ * conversion to D's type [EW]:  NONE: D = acc;  ADD_SCALAR: D = acc + s. */
+enum { TG_EPI_NONE = 0, TG_EPI_ADD_SCALAR = 1 };
+
+/* Launch flags (bit set). */
+enum {
+  TG_FLAG_CTA_PAIR = 1u /* cta_group::2: two CTAs of a cluster share one
+                           256-row MMA; each loads half of the B tile */
+};
+
+/*
+ * gemm_bf16 -- D[M,N] = A[M,K] * B[N,K]^T (+ epilogue), bf16 inputs, f32
+ * accumulation in tensor memory [MMA].
+ *   A    : device, bf16 [M, K], row stride lda (elements), K-major.
+ *   B    : device, bf16 [N, K], row stride ldb, K-major.
+ *   D    : device, [M, N] of d_dtype (TG_D_F32 or TG_D_BF16), row stride ldd.
+ *   M,N,K: sizes, 0 <= M, N, K < 2^31.  M or N == 0: nothing is launched.
+ *          K == 0: D = epilogue(0).  Any size need not be a tile multiple:
+ *          loads past the edge read zeros [TMA], stores past it are dropped.
+ *   epilogue, epi_scalar: TG_EPI_NONE or TG_EPI_ADD_SCALAR with constant s.
+ *   flags: 0 or TG_FLAG_CTA_PAIR.
+ * Rounding: f32 -> bf16 D is round-to-nearest-even.  Alignment: A, B, D
+ * 16-byte aligned; lda*2, ldb*2, ldd*sizeof(D) multiples of 16.
+ * Returns TG_OK once the kernel is enqueued, else an error (nothing enqueued).
+ */
+int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+              int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue, float epi_scalar,
+              unsigned flags, void* cuda_stream);
+
+/*
+ * gemm_mxfp8_blockscaled -- block-scaled MXFP8 product [MMA, .block_scale]:
+ *   D[i,j] = sum_k (A[i,k] * 2^(SFA[i,k/32]-127)) * (B[j,k] * 2^(SFB[j,k/32]-127))
+ *   A   : device, FP8 E4M3FN bytes [M, K], row stride lda (bytes).
+ *   B   : device, FP8 E4M3FN bytes [N, K], row stride ldb.
+ *   SFA : device, E8M0 bytes [M, K/32], row stride ld_sfa (any value >= K/32).
+ *   SFB : device, E8M0 bytes [N, K/32], row stride ld_sfb.
+ *   D, ldd, d_dtype, epilogue, epi_scalar, flags: as for gemm_bf16.
+ *   K must be a multiple of 32 (one scale per 32 K elements); otherwise
+ *   TG_ERR_INVALID_ARG.  lda and ldb must be multiples of 16.
+ * The scales are first rearranged on the device into the tensor-memory image
+ * the MMA reads (row r -> lane r%32, byte column 4*(r/32)) in a library-owned
+ * per-device workspace of ceil(M/128)*ceil(K/128)*512 + ceil(N/128)*
+ * ceil(K/128)*512 bytes; calls that overlap in time on different streams of
+ * one device share that workspace and must not be issued concurrently.
+ */
+int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           int epilogue, float epi_scalar, unsigned flags, void* cuda_stream);
+
+/*
+ * tile_transpose_b16 -- out[j,i] = in[i,j] for 16-bit elements, bit-exact
+ * (raw bit patterns, NaNs included) [LDM].  Built from ldmatrix.trans and
+ * stmatrix through shared memory.
+ *   in  : device, [rows, cols] 16-bit, row stride ld_in (elements).
+ *   out : device, [cols, rows] 16-bit, row stride ld_out.  Must not overlap in.
+ *   rows, cols >= 0 (0: nothing launched).  Pointers 16-byte aligned;
+ *   ld_in and ld_out multiples of 8.
+ */
+int tile_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out, int64_t rows,
+                       int64_t cols, void* cuda_stream);
+
+/*
+ * tg_device_status -- synchronise `cuda_stream`, then return and clear the
+ * current device's status word: TG_OK, or TG_ERR_TIMEOUT when a kernel's
+ * pipeline wait passed its deadline (the kernel then stopped early, left its
+ * outputs incomplete and released its tensor memory), or TG_ERR_CUDA when
+ * the synchronisation itself failed.  `site` (may be NULL) receives the code
+ * of the wait that expired.
+ */
+int tg_device_status(void* cuda_stream, uint32_t* site);
+
+/* Deadline of every bounded pipeline wait, in nanoseconds (default 2e9).
+ * Applies to launches made after the call; 0 is rejected. */
+int tg_set_wait_timeout_ns(uint64_t ns);
+
+/* Static string for a tg_status value. */
+const char* tg_status_string(int status);
+
+/* The cudaError_t behind the most recent TG_ERR_CUDA returned on this thread. */
+int tg_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

@@ -1,0 +1,68 @@
+/*
+ * tgemm probes -- small single-CTA kernels that run the pages' worked
+ * examples and dump raw hardware mappings, so that each building block of
+ * the GEMM and transpose path can be checked on its own against the CPU
+ * oracle.  They are part of libtgemm.so; they are not on the GEMM path.
+ *
+ * All pointers are device pointers owned by the caller; every call is
+ * asynchronous on `cuda_stream` and returns a tg_status (tgemm.h) before
+ * launching anything if an argument is wrong.
+ */
+#ifndef TGEMM_PROBES_H
+#define TGEMM_PROBES_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* "Tile Operands and Execution", section "A Load, Compute, and Store
+ * Example": 64 threads, each loads twelve f32 with three ld.global.v4.b32,
+ * adds one, stores with st.global.v4.b32.  a, b: f32 [2, 32, 3, 4], 16-byte
+ * aligned. */
+int tg_probe_add_one_v4(const float* a, float* b, void* cuda_stream);
+
+/* "ldmatrix / stmatrix", section "Example: interleaved shared rows and
+ * register slots 0, 2, 8, 10": x: uint32 [16, 4, 2] is placed in shared
+ * memory with strides (8, 1, 128) words; every lane fills twelve registers
+ * with 4294966519 and issues two ldmatrix .x2 on the (k, m, r, w) view
+ * SM[2r+m, w, k]; out: uint32 [32, 12] receives each lane's registers. */
+int tg_probe_ldmatrix_x2_interleaved(const uint32_t* x, uint32_t* out, void* cuda_stream);
+
+/* ldmatrix.m8n8.x{n}[.trans].shared.b16 of n matrices stored as rows:
+ * smem_image: uint16 [n, 8, 8] (matrix, row, column); out: uint32 [32, n],
+ * word i of lane l.  n in {1, 2, 4}, trans in {0, 1}. */
+int tg_probe_ldmatrix(const uint16_t* smem_image, int n, int trans, uint32_t* out,
+                      void* cuda_stream);
+
+/* stmatrix.m8n8.x{n}[.trans].shared.b16: regs: uint32 [32, n] (word i of
+ * lane l); out: uint16 [n, 8, 8], the shared rows written. */
+int tg_probe_stmatrix(const uint32_t* regs, int n, int trans, uint16_t* out, void* cuda_stream);
+
+/* "cp.async.bulk.tensor", section "Example: two explicit 8x16 boxes": one
+ * lane loads a (16, 16) uint32 tensor as two 8x16 TMA boxes at (0, 0) and
+ * (8, 0) on one barrier phase expecting 1024 bytes.  a, out: uint32 [16, 16]. */
+int tg_probe_tma_two_boxes(const uint32_t* a, uint32_t* out, void* cuda_stream);
+
+/* One TMA load of a bf16 [rows, 64] box with 128-byte swizzle; out receives
+ * the raw shared-memory bytes (rows * 128).  rows in 8..256, multiple of 8. */
+int tg_probe_tma_swizzle128(const uint16_t* src, int rows, uint8_t* out, void* cuda_stream);
+
+/* "tcgen05.mma", section "Example: four K16 issues for a 128x64x64 product",
+ * in bf16: a: bf16 [128, 64] and b: bf16 [64, 64] (B stored as (N, K)) are
+ * written to 128-byte-swizzled K-major shared layouts with ordinary stores,
+ * one thread issues four kind::f16 M128 N64 K16 MMAs and one commit, four
+ * warps read TMEM back with tcgen05.ld 32x32b; out: f32 [128, 64] = a @ b.T. */
+int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, void* cuda_stream);
+
+/* Waits on an mbarrier that nothing completes, with deadline `timeout_ns`
+ * (1..10^9); the bounded wait gives up and records TG_ERR_TIMEOUT with site
+ * code 99 in the status word that tg_device_status() returns. */
+int tg_probe_wait_timeout(uint64_t timeout_ns, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_PROBES_H */

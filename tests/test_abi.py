@@ -1,0 +1,101 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import blackwell_tile_gemm_gb300 as tg
+from blackwell_tile_gemm_gb300 import build as tgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("tgemm.h", "tgemm_probes.h")]
+
+
+@pytest.fixture(scope="module")
+def L():
+    tgbuild.build()
+    return tg.lib()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_headers_declare_the_three_entry_points():
+    names = declared_functions()
+    for n in ("gemm_bf16", "gemm_mxfp8_blockscaled", "tile_transpose_b16", "tg_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(L):
+    assert tg.status_string(0) == "ok"
+    assert "misaligned" in tg.status_string(2)
+    assert L.tg_version() >= 100
+
+
+def test_zero_timeout_is_rejected(L):
+    assert L.tg_set_wait_timeout_ns(0) == tg.TG_ERR_INVALID_ARG
+
+
+A16 = 0x10000           # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), tg.TG_ERR_INVALID_ARG),
+    (dict(K=-5), tg.TG_ERR_INVALID_ARG),
+    (dict(d_dtype=7), tg.TG_ERR_INVALID_ARG),
+    (dict(epilogue=9), tg.TG_ERR_INVALID_ARG),
+    (dict(flags=0x80), tg.TG_ERR_UNSUPPORTED),
+    (dict(A=0), tg.TG_ERR_INVALID_ARG),
+    (dict(D=0), tg.TG_ERR_INVALID_ARG),
+    (dict(lda=32), tg.TG_ERR_INVALID_ARG),          # lda < K
+    (dict(A=A16 + 2), tg.TG_ERR_MISALIGNED),
+    (dict(D=A16 + 8), tg.TG_ERR_MISALIGNED),
+    (dict(lda=68), tg.TG_ERR_MISALIGNED),           # 136 bytes, not a multiple of 16
+    (dict(ldd=66, N=66), tg.TG_ERR_MISALIGNED),     # f32 D: 264 bytes
+])
+def test_gemm_bf16_rejects_before_launch(L, kw, code):
+    a = dict(A=A16, lda=64, B=A16, ldb=64, D=A16, ldd=64, M=64, N=64, K=64, d_dtype=0,
+             epilogue=0, s=0.0, flags=0)
+    a.update(kw)
+    rc = L.gemm_bf16(a["A"], a["lda"], a["B"], a["ldb"], a["D"], a["ldd"], a["M"], a["N"],
+                     a["K"], a["d_dtype"], a["epilogue"], a["s"], a["flags"], None)
+    assert rc == code
+
+
+def test_empty_problems_return_ok_without_cuda(L):
+    assert L.gemm_bf16(0, 0, 0, 0, 0, 0, 0, 64, 64, 0, 0, 0.0, 0, None) == tg.TG_OK
+    assert L.gemm_bf16(0, 0, 0, 0, 0, 0, 64, 0, 64, 0, 0, 0.0, 0, None) == tg.TG_OK
+    assert L.tile_transpose_b16(0, 0, 0, 0, 0, 5, None) == tg.TG_OK
+
+
+def test_mxfp8_rejects_bad_k_and_scales(L):
+    f = L.gemm_mxfp8_blockscaled
+    # K not a multiple of 32
+    assert f(A16, 48, A16, 48, A16, 2, A16, 2, A16, 64, 64, 64, 48, 0, 0, 0.0, 0, None) == 1
+    # missing scales
+    assert f(A16, 64, A16, 64, 0, 2, A16, 2, A16, 64, 64, 64, 64, 0, 0, 0.0, 0, None) == 1
+    # scale row stride shorter than K/32
+    assert f(A16, 64, A16, 64, A16, 1, A16, 2, A16, 64, 64, 64, 64, 0, 0, 0.0, 0, None) == 1
+    # lda = 40 bytes is not a multiple of 16
+    assert f(A16, 40, A16, 64, A16, 2, A16, 2, A16, 64, 64, 64, 32, 0, 0, 0.0, 0, None) == 2
+
+
+def test_transpose_rejects_bad_arguments(L):
+    f = L.tile_transpose_b16
+    assert f(A16, 12, A16 * 4, 64, 64, 12, None) == tg.TG_ERR_MISALIGNED     # ld_in % 8
+    assert f(A16 + 2, 64, A16 * 4, 64, 64, 64, None) == tg.TG_ERR_MISALIGNED
+    assert f(A16, 32, A16 * 4, 64, 64, 64, None) == tg.TG_ERR_INVALID_ARG    # ld_in < cols
+    assert f(A16, 64, A16 + 64, 64, 64, 64, None) == tg.TG_ERR_INVALID_ARG  # overlap
