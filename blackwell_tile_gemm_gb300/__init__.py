@@ -28,6 +28,7 @@ TG_ERR_MISALIGNED = 2
 TG_ERR_UNSUPPORTED = 3
 TG_ERR_CUDA = 4
 TG_ERR_TIMEOUT = 5
+TG_ERR_NO_SCRATCH = 6
 TG_D_F32 = 0
 TG_D_BF16 = 1
 TG_EPI_NONE = 0
@@ -66,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_mxfp8_blockscaled.restype = i32
         L.gemm_mxfp8_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                              i64, i64, i64, i32, i32, ctypes.c_float, u32, vp]
+        L.gemm_mxfp8_blockscaled_noalloc.restype = i32
+        L.gemm_mxfp8_blockscaled_noalloc.argtypes = list(L.gemm_mxfp8_blockscaled.argtypes)
         L.tile_transpose_b16.restype = i32
         L.tile_transpose_b16.argtypes = [vp, i64, vp, i64, i64, i64, vp]
         L.tg_device_status.restype = i32
@@ -181,6 +184,30 @@ def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_a
         D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
         float(epilogue_add or 0.0), TG_FLAG_CTA_PAIR if cta_pair else 0, _stream_handle(stream))
     _check(rc, "gemm_mxfp8_blockscaled")
+    return D
+
+
+def gemm_mxfp8_blockscaled_noalloc(A, B, SFA, SFB, D, *, epilogue_add=None, cta_pair=False,
+                                   stream=None):
+    """``gemm_mxfp8_blockscaled`` for callers that must not allocate device memory.
+
+    Same arguments and result, except that D must be supplied (this call
+    allocates nothing, not even its output).  The scale rearrangement uses a
+    fixed 8 MiB scratch array built into the library instead of an allocated
+    workspace; problems that need more raise TgError(TG_ERR_NO_SCRATCH).
+    Calls that may overlap on the GPU share that scratch and race.
+    """
+    M, K = A.shape
+    N = B.shape[0]
+    if tuple(D.shape) != (M, N):
+        raise ValueError("D must be [M, N]")
+    epi = TG_EPI_NONE if epilogue_add is None else TG_EPI_ADD_SCALAR
+    rc = lib().gemm_mxfp8_blockscaled_noalloc(
+        A.data_ptr(), _ld(A, "A", 16), B.data_ptr(), _ld(B, "B", 16),
+        SFA.data_ptr(), _ld(SFA, "SFA", 1), SFB.data_ptr(), _ld(SFB, "SFB", 1),
+        D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
+        float(epilogue_add or 0.0), TG_FLAG_CTA_PAIR if cta_pair else 0, _stream_handle(stream))
+    _check(rc, "gemm_mxfp8_blockscaled_noalloc")
     return D
 
 

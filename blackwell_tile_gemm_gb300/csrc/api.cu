@@ -191,6 +191,24 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+namespace tg {
+
+// Argument checks of the block-scaled call, shared with the variant that
+// takes its scratch from a static array (gemm_mxfp8_noalloc.cu).
+int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb, const void* SFA,
+                     int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D, int64_t ldd,
+                     int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
+                     unsigned flags) {
+  if (K % 32 != 0) return TG_ERR_INVALID_ARG;
+  int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 1);
+  if (rc != TG_OK || M == 0 || N == 0) return rc;
+  if (K > 0 && (SFA == nullptr || SFB == nullptr || ld_sfa < K / 32 || ld_sfb < K / 32))
+    return TG_ERR_INVALID_ARG;
+  return TG_OK;
+}
+
+}  // namespace tg
+
 extern "C" {
 
 int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
@@ -269,6 +287,7 @@ const char* tg_status_string(int status) {
     case TG_ERR_UNSUPPORTED: return "unsupported request";
     case TG_ERR_CUDA: return "CUDA error";
     case TG_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case TG_ERR_NO_SCRATCH: return "problem needs more scratch than the static no-allocation buffer";
     default: return "unknown status";
   }
 }

@@ -53,6 +53,12 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
                            float epi_scalar, bool pair, uint8_t* sf_workspace,
                            cudaStream_t stream, DeviceCtx* ctx);
 
+// Host-side argument checks of the block-scaled call (no CUDA calls).
+int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb, const void* SFA,
+                     int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D, int64_t ldd,
+                     int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
+                     unsigned flags);
+
 // Bytes of scale-image workspace the MXFP8 path needs for this problem.
 size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair);
 

@@ -50,7 +50,9 @@ typedef enum {
   TG_ERR_MISALIGNED = 2,  /* pointer or row stride violates the 16-byte rule  */
   TG_ERR_UNSUPPORTED = 3, /* valid request outside what is implemented         */
   TG_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                 */
-  TG_ERR_TIMEOUT = 5      /* (device) a pipeline wait passed its deadline      */
+  TG_ERR_TIMEOUT = 5,     /* (device) a pipeline wait passed its deadline      */
+  TG_ERR_NO_SCRATCH = 6   /* problem too large for the static scratch of
+                             gemm_mxfp8_blockscaled_noalloc                    */
 } tg_status;
 
 /* Element type of D. */
@@ -105,6 +107,32 @@ int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ld
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
                            int epilogue, float epi_scalar, unsigned flags, void* cuda_stream);
+
+/*
+ * gemm_mxfp8_blockscaled_noalloc -- the same product as gemm_mxfp8_blockscaled,
+ * for callers that must not allocate device memory (a host framework whose
+ * own pool owns the device memory, a latency-bound serving loop where
+ * cudaMalloc/cudaFree would synchronise the device, a deployment that
+ * forbids allocation after start-up).  The pages have no counterpart: this
+ * is a library-usage variant, not part of the method.
+ *   Arguments, layouts, alignment rules and results: as gemm_mxfp8_blockscaled.
+ *   Scratch: a fixed 8 MiB device array inside the library (reserved on every
+ *   GPU that loads it, until the process exits) instead of the allocated
+ *   workspace.  The call never calls cudaMalloc or cudaFree.  A problem needs
+ *   (ceil(M/r)*(r/128) + 2*ceil(N/256)) * ceil(K/128) * 512 bytes of it, with
+ *   r = 256 under TG_FLAG_CTA_PAIR and 128 otherwise (4 MiB at 8192^3);
+ *   larger problems return TG_ERR_NO_SCRATCH and launch nothing.
+ *   Sharing: every call on a device uses the same array.  Calls whose kernels
+ *   may overlap on the GPU (unordered streams) race on it.  Each call rewrites
+ *   all scratch it reads, so leftover contents from an earlier call are harmless.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   with that device current; make that first call before any stream capture.
+ */
+int gemm_mxfp8_blockscaled_noalloc(const void* A, int64_t lda, const void* B, int64_t ldb,
+                                   const void* SFA, int64_t ld_sfa, const void* SFB,
+                                   int64_t ld_sfb, void* D, int64_t ldd, int64_t M, int64_t N,
+                                   int64_t K, int d_dtype, int epilogue, float epi_scalar,
+                                   unsigned flags, void* cuda_stream);
 
 /*
  * tile_transpose_b16 -- out[j,i] = in[i,j] for 16-bit elements, bit-exact

@@ -1,0 +1,72 @@
+"""gemm_mxfp8_blockscaled_noalloc: the block-scaled GEMM for callers that must
+not allocate device memory (a framework whose pool owns the device memory, a
+latency-bound loop where cudaMalloc/cudaFree would synchronise the device, a
+deployment that forbids allocation after start-up).  It takes its scratch
+from a fixed 8 MiB array built into the library.
+
+The GPU test calls the new entry point through the C ABI twice in a row, on
+two different problems, and checks each result against the regular entry
+point (gemm_mxfp8_blockscaled) on the same inputs, within the tolerance the
+other parity tests use.  The file name sorts last so that a run that stops at
+the first failure has already run every other test; it also passes alone in a
+fresh process, where its first call performs the per-device set-up.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import blackwell_tile_gemm_gb300 as tg
+from blackwell_tile_gemm_gb300 import build as tgbuild
+from blackwell_tile_gemm_gb300 import synth
+
+A16 = 0x10000      # a 16-byte aligned stand-in address, never dereferenced
+
+
+def _raw_call(L, A, B, SFA, SFB, D, pair, stream):
+    M, K = A.shape
+    N = B.shape[0]
+    return L.gemm_mxfp8_blockscaled_noalloc(
+        A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), SFA.data_ptr(), SFA.stride(0),
+        SFB.data_ptr(), SFB.stride(0), D.data_ptr(), D.stride(0), M, N, K,
+        tg.TG_D_F32 if D.dtype.itemsize == 4 else tg.TG_D_BF16, tg.TG_EPI_ADD_SCALAR, 0.5,
+        tg.TG_FLAG_CTA_PAIR if pair else 0, ctypes.c_void_p(stream.cuda_stream))
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    # 16384 x 16384 x 16384 in CTA pairs needs (128 + 128) * 128 * 512 bytes =
+    # 16 MiB of scale images, twice the scratch; rejected before any CUDA call.
+    tgbuild.build()
+    L = tg.lib()
+    rc = L.gemm_mxfp8_blockscaled_noalloc(A16, 16384, A16, 16384, A16, 512, A16, 512, A16, 16384,
+                                          16384, 16384, 16384, 1, 0, 0.0, 1, None)
+    assert rc == tg.TG_ERR_NO_SCRATCH
+    assert "scratch" in tg.status_string(rc)
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_allocating_entry_point_twice_in_a_row(oracle):
+    from tests._gpu import BF16_ATOL, BF16_RTOL, F32_ATOL, F32_RTOL, dev_u8, host_values, worst_ratio
+    from tests._gpu import torch_cuda
+    torch = torch_cuda()
+    L = tg.lib()
+    stream = torch.cuda.current_stream()
+    cases = [
+        # (M, N, K, D dtype, CTA pairs, seed): two different problems in a row,
+        # so the second call runs over scratch the first one left behind.
+        (512, 768, 1024, torch.bfloat16, True, 71),
+        (300, 264, 160, torch.float32, False, 72),
+    ]
+    for M, N, K, dt, pair, seed in cases:
+        x = synth.make_inputs("mx8k", M=M, N=N, K=K, seed=seed)
+        A, B, SFA, SFB = (dev_u8(x[k]) for k in ("A", "B", "SFA", "SFB"))
+        D_new = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+        D_ref = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+        assert _raw_call(L, A, B, SFA, SFB, D_new, pair, stream) == tg.TG_OK
+        tg.gemm_mxfp8_blockscaled(A, B, SFA, SFB, D_ref, epilogue_add=0.5, cta_pair=pair)
+        assert tg.tg_device_status() == (tg.TG_OK, 0)
+        got, want = host_values(D_new), host_values(D_ref)
+        _, mag = oracle.gemm_mxfp8(x["A"], x["B"], x["SFA"], x["SFB"])
+        rtol, atol = (F32_RTOL, F32_ATOL) if dt == torch.float32 else (BF16_RTOL, BF16_ATOL)
+        ratio, idx = worst_ratio(got, want, mag, rtol, atol)
+        assert ratio <= 1.0, (M, N, K, idx, got[idx], want[idx])
