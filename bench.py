@@ -167,19 +167,26 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream()
     host, d = make_step_inputs(torch, dev)
     flops_gemm = 2 * SIZE ** 3
-    flops_step = 2 * flops_gemm
+
+    run_bf16 = args.kernel in ("all", "gemm_bf16")
+    run_mx = args.kernel in ("all", "gemm_mxfp8")
+    run_tr = args.kernel in ("all", "transpose")
+    flops_step = flops_gemm * (int(run_bf16) + int(run_mx))
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        tg.gemm_bf16(d["A"], d["B"], d["D"], cta_pair=True, stream=stream)
+        if run_bf16:
+            tg.gemm_bf16(d["A"], d["B"], d["D"], cta_pair=True, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        tg.gemm_mxfp8_blockscaled(d["mA"], d["mB"], d["SFA"], d["SFB"], d["mD"], cta_pair=True,
-                                  stream=stream)
+        if run_mx:
+            tg.gemm_mxfp8_blockscaled(d["mA"], d["mB"], d["SFA"], d["SFB"], d["mD"],
+                                      cta_pair=True, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        tg.tile_transpose_b16(d["X"], d["XT"], stream=stream)
+        if run_tr:
+            tg.tile_transpose_b16(d["X"], d["XT"], stream=stream)
         if ev is not None:
             ev[3].record(stream)
 
@@ -210,47 +217,59 @@ def run_ours(args, rank, world, local):
                     for e in evs])
     total_ms = reduce_max(total_ms, world)
     ms_step = total_ms / args.steps
-    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    if flops_step:
+        value = flops_step * world / (ms_step * 1e-3) / 1e12
+    else:   # transpose alone: report its bandwidth instead
+        value = 2 * 2 * SIZE * SIZE * world / (ms_step * 1e-3) / 1e9
 
     peaks, peak_src = measured_peaks()
     bf16_ms, mx_ms, tr_ms = (float(per[:, i].mean()) for i in range(3))
     peak_bf16 = float(peaks["bf16_tflops"])
-    kern = {
-        "gemm_bf16": {"ms": bf16_ms, "tflops": flops_gemm / (bf16_ms * 1e-3) / 1e12},
-        "gemm_mxfp8_blockscaled": {"ms": mx_ms, "tflops": flops_gemm / (mx_ms * 1e-3) / 1e12},
-        "tile_transpose_b16": {"ms": tr_ms, "gbs": 2 * 2 * SIZE * SIZE / (tr_ms * 1e-3) / 1e9},
-    }
-    kern["gemm_bf16"]["frac_of_bf16_peak"] = kern["gemm_bf16"]["tflops"] / peak_bf16
-    kern["gemm_mxfp8_blockscaled"]["frac_of_2x_bf16_peak"] = (
-        kern["gemm_mxfp8_blockscaled"]["tflops"] / (2 * peak_bf16))
-    kern["tile_transpose_b16"]["frac_of_hbm_peak"] = (
-        kern["tile_transpose_b16"]["gbs"] / float(peaks["hbm_gbs"]))
-    dominant = max(("gemm_bf16", "gemm_mxfp8_blockscaled"), key=lambda n: kern[n]["ms"])
-    if dominant == "gemm_bf16":
+    kern = {}
+    if run_bf16:
+        t = flops_gemm / (bf16_ms * 1e-3) / 1e12
+        kern["gemm_bf16"] = {"ms": bf16_ms, "tflops": t, "frac_of_bf16_peak": t / peak_bf16}
+    if run_mx:
+        t = flops_gemm / (mx_ms * 1e-3) / 1e12
+        kern["gemm_mxfp8_blockscaled"] = {"ms": mx_ms, "tflops": t,
+                                          "frac_of_2x_bf16_peak": t / (2 * peak_bf16)}
+    if run_tr:
+        g = 2 * 2 * SIZE * SIZE / (tr_ms * 1e-3) / 1e9
+        kern["tile_transpose_b16"] = {"ms": tr_ms, "gbs": g,
+                                      "frac_of_hbm_peak": g / float(peaks["hbm_gbs"])}
+    dominant = max(kern, key=lambda n: kern[n]["ms"])
+    if dominant == "tile_transpose_b16":
+        achieved, peak = kern[dominant]["gbs"], float(peaks["hbm_gbs"])
+        peak_note = f"HBM copy, {peak_src}"
+    elif dominant == "gemm_bf16":
         achieved, peak = kern["gemm_bf16"]["tflops"], peak_bf16
         peak_note = f"bf16 cuBLAS burst, {peak_src}"
     else:
         achieved, peak = kern[dominant]["tflops"], 2 * peak_bf16
         peak_note = f"2 x bf16 cuBLAS burst (fp8/bf16 nominal ratio), {peak_src}"
-    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+    roofline = {"bound": "hbm" if dominant == "tile_transpose_b16" else "tensor",
+                "kernel": dominant, "achieved": achieved, "peak": peak,
+                "unit": "GB/s" if dominant == "tile_transpose_b16" else "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
                 "peak_source": peak_note}
 
-    e2e = measure_e2e(torch, tg, host, dev, stream, args.e2e_steps, flops_step)
+    e2e = measure_e2e(torch, tg, host, dev, stream, args.e2e_steps if args.kernel == "all" else 0,
+                      flops_step)
     cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1 and args.cpu_seconds > 0) \
         else None
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT if flops_step else "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3 (f32 accumulate)",
         "data": "synthetic (seeded numpy; recipes in blackwell_tile_gemm_gb300/synth.py)",
-        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
+        "config": {"workload": WORKLOAD if args.kernel == "all" else f"{args.kernel} only",
+                   "M": SIZE, "N": SIZE, "K": SIZE,
                    "tiles": "256x256 per CTA pair, 128-byte K stages",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "not flushed: 516 MB of step inputs > 129 MB L2"},
         "roofline": roofline, "kernels": kern, "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (int(run_bf16) + 2 * int(run_mx) + int(run_tr)) * args.steps,
         "clocks": clk.summary(),
     }
     if cpu is not None:
@@ -378,7 +397,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded numpy; recipes in blackwell_tile_gemm_gb300/synth.py)",
-        "config": {"workload": WORKLOAD, "M": SIZE, "N": SIZE, "K": SIZE,
+        "config": {"workload": WORKLOAD if args.kernel == "all" else f"{args.kernel} only",
+                   "M": SIZE, "N": SIZE, "K": SIZE,
                    "parallelism": "host cores (OpenMP over output rows)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -431,6 +451,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--kernel", choices=["all", "gemm_bf16", "gemm_mxfp8", "transpose"],
+                    default="all", help="run one part of the step only (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -10,6 +10,8 @@
 namespace tg {
 
 namespace {
+// m-tiles per band of the persistent tile order.
+constexpr int kRasterGroup = 8;
 using CfgF32 = GemmCfg<1, false, 256, 2, 4, false>;
 using CfgBf16 = GemmCfg<1, false, 256, 2, 4, true>;
 using CfgPairF32 = GemmCfg<2, false, 256, 2, 6, false>;
@@ -40,6 +42,7 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
   a.ldd = ldd;
   a.epi_scalar = epi_scalar;
   a.epi_add = epi_add;
+  a.raster_group = kRasterGroup;
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
   const bool bf16_out = d_dtype == TG_D_BF16;

@@ -17,9 +17,10 @@
 //               (copies the scale images into TMEM,) issues the K16 / K32
 //               MMAs, and commits to the slot's "empty" barrier; at the end of
 //               a tile it commits to the accumulator's "full" barrier.
-//   warps 2..5  epilogue: wait for a full accumulator, tcgen05.ld 32 columns
-//               at a time (row = TMEM lane), apply the scalar op, convert and
-//               store with st.global.v4; release the accumulator.
+//   warps 2..9  epilogue: wait for a full accumulator; each warp reads its
+//               32 TMEM lanes x BN/2 columns with tcgen05.ld (row = lane) into
+//               registers and releases the accumulator at once, then applies
+//               the scalar op, converts and stores with st.global.v4.
 //
 // Tiles are visited persistently (one CTA or CTA pair per SM, static stride)
 // in grouped order so that CTAs running at the same time share A and B panels
@@ -51,6 +52,7 @@ struct GemmArgs {
   int epi_add;      // 0: D = acc; 1: D = acc + epi_scalar
   int sfa_blocks;   // 128-row blocks per K group in the SFA image
   int sfb_blocks;   // 128-row blocks per K group in the SFB image
+  int raster_group; // m-tiles per band of the tile order
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -95,21 +97,27 @@ struct GemmCfg {
                                    : TMEM_USED <= 256 ? 256
                                                       : 512;
   static constexpr uint32_t MMA_M = BM * kCtaGroup;
-  static constexpr int kThreads = 192;
+  // Epilogue: 8 warps; warp w reads TMEM lanes 32*(w%4).. and one half of the
+  // BN columns, holding that half (BN/2 f32 per thread) in registers.
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiCols = BN / 2;
+  static constexpr int kEpiChunks = kEpiCols / 32;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
 };
 
-// Grouped tile order: consecutive tile ids walk down a band of kGroup m-tiles
-// before moving to the next n-tile.
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& tm, int& tn) {
-  constexpr int kGroup = 16;
-  const int per_group = kGroup * num_n;
+// Grouped tile order: consecutive tile ids walk down a band of `group`
+// m-tiles before moving to the next n-tile, so the CTAs that run at the same
+// time share a few A and B panels in L2.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group, int& tm,
+                                            int& tn) {
+  const int per_group = group * num_n;
   const int g = t / per_group;
-  const int first_m = g * kGroup;
-  const int gm = min(num_m - first_m, kGroup);
+  const int first_m = g * group;
+  const int gm = min(num_m - first_m, group);
   const int r = t - g * per_group;
   tm = first_m + r % gm;
   tn = r / gm;
@@ -117,7 +125,7 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& tm
 
 template <class C>
 __device__ __forceinline__ void epilogue_store_chunk(const GemmArgs& p, int row, int col0,
-                                                     const uint32_t (&v)[32]) {
+                                                     const uint32_t (&v)[32], uint64_t pol) {
   const float add = p.epi_add ? p.epi_scalar : 0.0f;
   if constexpr (C::kBf16Out) {
     uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + static_cast<int64_t>(row) * p.ldd;
@@ -128,13 +136,14 @@ __device__ __forceinline__ void epilogue_store_chunk(const GemmArgs& p, int row,
     if (col0 + 32 <= p.N) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        st_global_v4(drow + col0 + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        st_global_v4_hint(drow + col0 + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3],
+                          pol);
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int c = col0 + 8 * i;
         if (c + 8 <= p.N) {
-          st_global_v4(drow + c, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          st_global_v4_hint(drow + c, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3], pol);
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -151,13 +160,14 @@ __device__ __forceinline__ void epilogue_store_chunk(const GemmArgs& p, int row,
     if (col0 + 32 <= p.N) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        st_global_v4(drow + col0 + 4 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        st_global_v4_hint(drow + col0 + 4 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3],
+                          pol);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c = col0 + 4 * i;
         if (c + 4 <= p.N) {
-          st_global_v4(drow + c, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          st_global_v4_hint(drow + c, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3], pol);
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&accf_bar[b], 1);
-      mbar_init(&acce_bar[b], 4 * C::kCtaGroup);
+      mbar_init(&acce_bar[b], C::kEpiWarps * C::kCtaGroup);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -227,6 +237,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int unit = blockIdx.x / C::kCtaGroup;         // CTA or CTA pair index
   const int num_units = gridDim.x / C::kCtaGroup;
 
+  // The producer and MMA loops run one thread each and are latency-critical:
+  // the tensor pipe queues only a couple of MMAs, so every instruction the
+  // MMA thread spends between issues can idle it.  Hence barrier checks take
+  // an inline fast path (one try_wait) and fall back to the bounded wait only
+  // when a barrier is not ready, shared-memory descriptors are advanced by
+  // adding offsets, and the next stage's barrier is probed while the current
+  // stage's MMAs are queued.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -235,44 +252,49 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t sB = smem_addr(smem + C::OFF_B);
       const uint32_t sSFA = smem_addr(smem + C::OFF_SFA);
       const uint32_t sSFB = smem_addr(smem + C::OFF_SFB);
+      const uint32_t empty0 = smem_addr(&empty_bar[0]);
+      const uint32_t full0 = smem_addr(&full_bar[0]);
+      // Pair: both CTAs' loads complete on the leader's barrier.
+      const uint32_t full_dst0 = C::kCtaGroup == 2 ? map_to_cta(full0, 0) : full0;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;   // per-stage bit masks
       bool ok = true;
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         int tm, tn;
-        tile_coords(t, p.num_m_tiles, p.num_n_tiles, tm, tn);
+        tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.raster_group, tm, tn);
         const int a_row = tm * C::MMA_M + static_cast<int>(rank) * C::BM;
         const int b_row = tn * C::BN + static_cast<int>(rank) * C::B_ROWS;
+        const int sfa_row = C::kCtaGroup == 2 ? tm * 2 + static_cast<int>(rank) : tm;
+        const int sfb_row = tn * (C::BN / 128);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, guard, kSiteProducerEmpty)) {
+          if (!mbar_try_wait(empty0 + 8u * stage, phase ^ 1u) &&
+              !mbar_wait(&empty_bar[stage], phase ^ 1u, guard, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
           const int kx = kb * C::BK;
+          const uint32_t fb = full_dst0 + 8u * stage;
           if constexpr (C::kCtaGroup == 1) {
-            const uint32_t fb = smem_addr(&full_bar[stage]);
             mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_TX);
             tma_load_2d(sA + stage * C::A_BYTES, &tmA, fb, kx, a_row, pol_ab);
             tma_load_2d(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
             if constexpr (C::kMx) {
-              tma_load_2d(sSFA + stage * C::SFA_BYTES, &tmSFA, fb, 0, kb * p.sfa_blocks + tm,
+              tma_load_2d(sSFA + stage * C::SFA_BYTES, &tmSFA, fb, 0, kb * p.sfa_blocks + sfa_row,
                           pol_ab);
-              tma_load_2d(sSFB + stage * C::SFB_BYTES, &tmSFB, fb, 0,
-                          kb * p.sfb_blocks + tn * (C::BN / 128), pol_ab);
+              tma_load_2d(sSFB + stage * C::SFB_BYTES, &tmSFB, fb, 0, kb * p.sfb_blocks + sfb_row,
+                          pol_ab);
             }
           } else {
-            // Both CTAs' loads complete on the leader's barrier; only the
-            // leader posts the expected byte count (for the pair).
-            const uint32_t fb = map_to_cta(smem_addr(&full_bar[stage]), 0);
+            // Only the leader posts the expected byte count (for the pair).
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_TX);
             tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, fb, kx, a_row, pol_ab);
             tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
             if constexpr (C::kMx) {
               tma_load_2d_pair(sSFA + stage * C::SFA_BYTES, &tmSFA, fb, 0,
-                               kb * p.sfa_blocks + tm * 2 + static_cast<int>(rank), pol_ab);
+                               kb * p.sfa_blocks + sfa_row, pol_ab);
               tma_load_2d_pair(sSFB + stage * C::SFB_BYTES, &tmSFB, fb, 0,
-                               kb * p.sfb_blocks + tn * (C::BN / 128), pol_ab);
+                               kb * p.sfb_blocks + sfb_row, pol_ab);
             }
           }
           issued |= 1u << stage;
@@ -293,66 +315,76 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      const uint32_t sA = smem_addr(smem + C::OFF_A);
-      const uint32_t sB = smem_addr(smem + C::OFF_B);
-      const uint32_t sSFA = smem_addr(smem + C::OFF_SFA);
-      const uint32_t sSFB = smem_addr(smem + C::OFF_SFB);
+      const uint32_t full0 = smem_addr(&full_bar[0]);
+      const uint32_t acce0 = smem_addr(&acce_bar[0]);
+      // K-major, 128-byte swizzled operands: 8-row groups 1024 bytes apart;
+      // the K16 / K32 slice k of a stage starts 32 * k bytes into each row.
+      const uint64_t adesc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kDescSwizzle128B);
+      const uint64_t bdesc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kDescSwizzle128B);
+      // Scale images: 32 rows x 16 bytes per tcgen05.cp, 8-row groups 128 bytes apart.
+      const uint64_t sfadesc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_SFA), 16, 128, kDescSwizzleNone);
+      const uint64_t sfbdesc0 =
+          make_smem_desc(smem_addr(smem + C::OFF_SFB), 16, 128, kDescSwizzleNone);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      bool ready = false;       // full barrier of `stage` already seen complete
       for (int t = unit; t < num_tiles && ok; t += num_units) {
-        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, guard, kSiteMmaAccEmpty)) {
+        if (!mbar_try_wait(acce0 + 8u * acc, acc_phase ^ 1u) &&
+            !mbar_wait(&acce_bar[acc], acc_phase ^ 1u, guard, kSiteMmaAccEmpty)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, guard, kSiteMmaFull)) {
+          if (!ready && !mbar_try_wait(full0 + 8u * stage, phase) &&
+              !mbar_wait(&full_bar[stage], phase, guard, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a0 = sA + stage * C::A_BYTES;
-          const uint32_t b0 = sB + stage * C::B_BYTES;
+          const int ns = stage + 1 == C::kStages ? 0 : stage + 1;
+          const uint32_t nph = stage + 1 == C::kStages ? phase ^ 1u : phase;
+          const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::A_BYTES >> 4));
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::B_BYTES >> 4));
           if constexpr (C::kMx) {
+            // Scales go to this stage's TMEM columns first; the MMAs read them.
             const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_STAGE_COLS;
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-            // 32 rows x 16 bytes per copy; rows 8 apart by 128 bytes.
             tmem_cp_32x128b_warpx4<C::kCtaGroup>(
-                sfa_t, make_smem_desc(sSFA + stage * C::SFA_BYTES, 16, 128, kDescSwizzleNone));
+                sfa_t, sfadesc0 + static_cast<uint64_t>(stage * (C::SFA_BYTES >> 4)));
 #pragma unroll
             for (int j = 0; j < C::BN / 128; ++j)
               tmem_cp_32x128b_warpx4<C::kCtaGroup>(
                   sfb_t + 4 * j,
-                  make_smem_desc(sSFB + stage * C::SFB_BYTES + 512 * j, 16, 128,
-                                 kDescSwizzleNone));
+                  sfbdesc0 + static_cast<uint64_t>(stage * (C::SFB_BYTES >> 4) + 32 * j));
 #pragma unroll
             for (int k = 0; k < C::kIssues; ++k) {
-              const uint64_t ad = make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B);
-              const uint64_t bd = make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B);
-              mma_mxf8<C::kCtaGroup>(d_tmem, ad, bd, idesc_mxf8_e4m3(C::MMA_M, C::BN, k, k),
-                                     sfa_t, sfb_t, (kb | k) != 0);
+              mma_mxf8<C::kCtaGroup>(d_tmem, ad + 2 * k, bd + 2 * k,
+                                     idesc_mxf8_e4m3(C::MMA_M, C::BN, k, k), sfa_t, sfb_t,
+                                     (kb | k) != 0);
+              if (k == 0) ready = mbar_try_wait(full0 + 8u * ns, nph);
             }
           } else {
 #pragma unroll
             for (int k = 0; k < C::kIssues; ++k) {
-              const uint64_t ad = make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B);
-              const uint64_t bd = make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B);
-              mma_bf16<C::kCtaGroup>(d_tmem, ad, bd, idesc_bf16_f32(C::MMA_M, C::BN),
-                                     (kb | k) != 0);
+              mma_bf16<C::kCtaGroup>(d_tmem, ad + 2 * k, bd + 2 * k,
+                                     idesc_bf16_f32(C::MMA_M, C::BN), (kb | k) != 0);
+              if (k == 0) ready = mbar_try_wait(full0 + 8u * ns, nph);
             }
           }
           if constexpr (C::kCtaGroup == 1)
             mma_commit(&empty_bar[stage]);
           else
             mma_commit_pair(&empty_bar[stage], 0x3);
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          stage = ns;
+          phase = nph;
         }
         if (!ok) break;
         if constexpr (C::kCtaGroup == 1)
@@ -377,27 +409,30 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int slab = warp & 3;                        // TMEM lanes 32*slab .. +31
+    const int half = (warp - 2) >> 2;                 // which BN/2 columns
     const int row_in_tile = slab * 32 + static_cast<int>(lane);
+    const uint64_t pol_d = policy_evict_first();      // D is written once: keep A/B in L2
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t acce_remote = 0;
     if constexpr (C::kCtaGroup == 2) acce_remote = map_to_cta(smem_addr(&acce_bar[0]), 0);
     for (int t = unit; t < num_tiles; t += num_units) {
       int tm, tn;
-      tile_coords(t, p.num_m_tiles, p.num_n_tiles, tm, tn);
-      if (!mbar_wait(&accf_bar[acc], acc_phase, guard, kSiteEpiAccFull)) break;
+      tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.raster_group, tm, tn);
+      // One lane waits for the accumulator; the others wait at the warp barrier.
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&accf_bar[acc], acc_phase, guard, kSiteEpiAccFull) ? 1 : 0;
+      got = __shfl_sync(0xFFFFFFFFu, got, 0);
+      if (!got) break;
       tc_fence_after_sync();
-      const int row = tm * C::MMA_M + static_cast<int>(rank) * C::BM + row_in_tile;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(slab * 32) << 16) +
-                             static_cast<uint32_t>(acc * C::ACC_COLS);
-#pragma unroll 1
-      for (int c = 0; c < C::BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(t_row + 32 * c, v);
-        tmem_ld_wait();
-        const int col0 = tn * C::BN + 32 * c;
-        if (row < p.M && col0 < p.N) epilogue_store_chunk<C>(p, row, col0, v);
-      }
+                             static_cast<uint32_t>(acc * C::ACC_COLS + half * C::kEpiCols);
+      // Read this warp's whole share of the accumulator, then hand the
+      // accumulator back to the MMA warp before converting and storing.
+      uint32_t v[C::kEpiChunks][32];
+#pragma unroll
+      for (int c = 0; c < C::kEpiChunks; ++c) tmem_ld_32x32b_x32(t_row + 32 * c, v[c]);
+      tmem_ld_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -405,6 +440,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           mbar_arrive(&acce_bar[acc]);
         else
           mbar_arrive_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+      }
+      const int row = tm * C::MMA_M + static_cast<int>(rank) * C::BM + row_in_tile;
+#pragma unroll
+      for (int c = 0; c < C::kEpiChunks; ++c) {
+        const int col0 = tn * C::BN + half * C::kEpiCols + 32 * c;
+        if (row < p.M && col0 < p.N) epilogue_store_chunk<C>(p, row, col0, v[c], pol_d);
       }
       if (++acc == C::kAccBufs) {
         acc = 0;

@@ -22,6 +22,8 @@
 namespace tg {
 
 namespace {
+// m-tiles per band of the persistent tile order.
+constexpr int kRasterGroup = 8;
 
 using CfgMxF32 = GemmCfg<1, true, 256, 1, 4, false>;
 using CfgMxBf16 = GemmCfg<1, true, 256, 1, 4, true>;
@@ -139,6 +141,7 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
   a.epi_add = epi_add;
   a.sfa_blocks = pl.sfa_blocks;
   a.sfb_blocks = pl.sfb_blocks;
+  a.raster_group = kRasterGroup;
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
   const bool bf16_out = d_dtype == TG_D_BF16;

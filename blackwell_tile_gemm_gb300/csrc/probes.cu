@@ -222,6 +222,82 @@ __global__ void __launch_bounds__(128) mma_128x64x64_kernel(const uint16_t* a, c
   }
 }
 
+// ------------------------------------------------- tensor-pipe rate (no memory)
+// One CTA per SM; one thread issues `iters` x 4 back-to-back M128 N256 MMAs
+// (K16 bf16, K32 block-scaled E4M3, or K32 dense E4M3) on shared-memory
+// operands that never change, commits once and waits.  out[2*cta] = SM clock
+// cycles and out[2*cta+1] = nanoseconds from the first issue to completion of
+// the last MMA.  The launch asks for more shared memory than two CTAs can
+// share, so each CTA has an SM (and its tensor memory) to itself.
+template <int kKind>
+__global__ void __launch_bounds__(128) mma_rate_kernel(int iters, unsigned long long* out,
+                                                       uint32_t* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t dyn[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sa = base;                 // 128 rows x 128 B
+  uint8_t* sb = base + 128 * 128;     // 256 rows x 128 B
+  uint8_t* ssf = sb + 256 * 128;      // 3 x 512 B scale images
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) tmem_alloc<1>(&tmem_slot, 512);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  // Small integers (0x3C00 pattern = 1.0 in bf16 pairs / 1.5 in E4M3 pairs),
+  // unit scales: no denormals, no NaNs.
+  for (int i = tid; i < (128 + 256) * 128 / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(sa)[i] = kKind == 0 ? 0x3F803F80u : 0x38383838u;
+  for (int i = tid; i < 3 * 512 / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(ssf)[i] = 0x7F7F7F7Fu;
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  bool ok = true;
+  if (tid == 0) {
+    const uint32_t a0 = smem_addr(sa), b0 = smem_addr(sb), f0 = smem_addr(ssf);
+    const uint32_t sfa = tmem + 256, sfb = tmem + 260;
+    if constexpr (kKind == 1) {
+      tmem_cp_32x128b_warpx4<1>(sfa, make_smem_desc(f0, 16, 128, kDescSwizzleNone));
+      tmem_cp_32x128b_warpx4<1>(sfb, make_smem_desc(f0 + 512, 16, 128, kDescSwizzleNone));
+      tmem_cp_32x128b_warpx4<1>(sfb + 4, make_smem_desc(f0 + 1024, 16, 128, kDescSwizzleNone));
+    }
+    const unsigned long long t0 = clock64();
+    const unsigned long long g0 = global_timer_ns();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t ad = make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B);
+        const uint64_t bd = make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B);
+        if constexpr (kKind == 0)
+          mma_bf16<1>(tmem, ad, bd, idesc_bf16_f32(128, 256), (it | k) != 0);
+        else if constexpr (kKind == 1)
+          mma_mxf8<1>(tmem, ad, bd, idesc_mxf8_e4m3(128, 256, k, k), sfa, sfb, (it | k) != 0);
+        else
+          mma_f8_dense(tmem, ad, bd, idesc_f8_e4m3_f32(128, 256), (it | k) != 0);
+      }
+    }
+    mma_commit(&bar);
+    const WaitGuard guard{status, &abort_flag, timeout_ns};
+    ok = mbar_wait(&bar, 0, guard, 93);
+    if (!ok) mbar_wait_drain(&bar, 0, timeout_ns);
+    out[2 * blockIdx.x] = ok ? clock64() - t0 : 0ull;
+    out[2 * blockIdx.x + 1] = ok ? global_timer_ns() - g0 : 0ull;
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc<1>(tmem, 512);
+  }
+}
+
 // --------------------------------------------------------------- wait timeout
 __global__ void wait_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -336,6 +412,32 @@ int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, voi
   if (e != cudaSuccess) return cuda_fail(e);
   mma_128x64x64_kernel<<<1, 128, smem, static_cast<cudaStream_t>(s)>>>(a, b, out, ctx->status,
                                                                        wait_timeout_ns());
+  return launched();
+}
+
+int tg_probe_mma_rate(int kind, int iters, int ctas, unsigned long long* cycles, void* s) {
+  if (kind < 0 || kind > 2 || iters < 1 || iters > (1 << 20) || ctas < 1 || ctas > 4096 ||
+      cycles == nullptr)
+    return TG_ERR_INVALID_ARG;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  const int smem = 120 * 1024;   // >= (128 + 256) * 128 + 3 * 512 + 1024; one CTA per SM
+  cudaStream_t st = static_cast<cudaStream_t>(s);
+  cudaError_t e = cudaSuccess;
+  if (kind == 0) {
+    e = cudaFuncSetAttribute(mma_rate_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      mma_rate_kernel<0><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
+  } else if (kind == 1) {
+    e = cudaFuncSetAttribute(mma_rate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      mma_rate_kernel<1><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
+  } else {
+    e = cudaFuncSetAttribute(mma_rate_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      mma_rate_kernel<2><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
   return launched();
 }
 

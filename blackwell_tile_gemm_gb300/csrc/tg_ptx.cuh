@@ -119,6 +119,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, but lets the hardware suspend the thread for up to `hint_ns` while
+// the phase is incomplete (it resumes as soon as the phase completes), so a
+// waiting warp does not keep polling shared memory.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------------------
 // bounded waiting and the error channel
 // ---------------------------------------------------------------------------
@@ -136,7 +152,7 @@ struct WaitGuard {
   uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ void report_timeout(const WaitGuard& g, uint32_t site) {
+__device__ __forceinline__ void report_timeout(const WaitGuard g, uint32_t site) {
   if (atomicCAS(g.status, kDevOk, kDevTimeout) == kDevOk) {
     g.status[1] = site;
     g.status[2] = blockIdx.x;
@@ -148,14 +164,14 @@ __device__ __forceinline__ void report_timeout(const WaitGuard& g, uint32_t site
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) when the deadline passes or another role of this CTA already gave
 // up; the first give-up writes the status word.  Never traps.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitGuard& g,
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitGuard g,
                                        uint32_t site) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t spin = 1; spin != 0; ++spin) {   // the counter itself bounds the loop
-    if (mbar_try_wait(a, parity)) return true;
-    if ((spin & 31u) == 0) {
+    if (mbar_try_wait_sleep(a, parity, 20000u)) return true;
+    if ((spin & 7u) == 0) {
       if (*g.abort_flag) return false;
       if (global_timer_ns() - t0 > g.timeout_ns) {
         report_timeout(g, site);
@@ -338,6 +354,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor for .kind::f8f6f4 (dense): D f32, A/B E4M3 (format
+// 0), both K-major; same field positions as the .kind::f16 form.
+__host__ __device__ constexpr uint32_t idesc_f8_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Instruction descriptor for .kind::mxf8f6f4.block_scale: A/B E4M3 (format 0),
 // both K-major, scale format E8M0 ([23] = 1), [4,6) B scale-factor id,
 // [29,31) A scale-factor id (the byte inside each 32-bit TMEM scale column).
@@ -394,6 +416,17 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
   }
+}
+
+// Dense FP8: D (+)= A * B^T with E4M3 inputs, f32 accumulate (no scales).
+__device__ __forceinline__ void mma_f8_dense(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Arrive once on `bar` when all previously issued tcgen05 async operations
@@ -545,6 +578,14 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
                                              uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                "r"(d)
+               : "memory");
+}
+
+// Same, with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void st_global_v4_hint(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a),
+               "r"(b), "r"(c), "r"(d), "l"(policy)
                : "memory");
 }
 

@@ -26,6 +26,7 @@ def _L():
             "tg_probe_tma_swizzle128": [vp, i32, vp, vp],
             "tg_probe_mma_128x64x64": [vp, vp, vp, vp],
             "tg_probe_wait_timeout": [ctypes.c_uint64, vp],
+            "tg_probe_mma_rate": [i32, i32, i32, vp, vp],
         }.items():
             f = getattr(L, name)
             f.restype = i32
@@ -73,3 +74,9 @@ def mma_128x64x64(a, b, out, stream=None):
 def wait_timeout(timeout_ns, stream=None):
     _check(_L().tg_probe_wait_timeout(int(timeout_ns), _stream_handle(stream)),
            "tg_probe_wait_timeout")
+
+
+def mma_rate(kind, iters, ctas, cycles, stream=None):
+    """Back-to-back tcgen05.mma rate probe; cycles: int64 CUDA tensor [2*ctas] (cycles, ns)."""
+    _check(_L().tg_probe_mma_rate(int(kind), int(iters), int(ctas), cycles.data_ptr(),
+                                  _stream_handle(stream)), "tg_probe_mma_rate")

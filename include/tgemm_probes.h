@@ -56,6 +56,18 @@ int tg_probe_tma_swizzle128(const uint16_t* src, int rows, uint8_t* out, void* c
  * warps read TMEM back with tcgen05.ld 32x32b; out: f32 [128, 64] = a @ b.T. */
 int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, void* cuda_stream);
 
+/* Tensor-pipe rate with no memory traffic: `ctas` CTAs (one per SM when
+ * ctas <= SM count), each issuing iters x 4 back-to-back M128 N256 MMAs on
+ * fixed shared-memory operands into one TMEM accumulator.  kind: 0 = bf16
+ * kind::f16 K16, 1 = E4M3 kind::mxf8f6f4.block_scale K32 (unit scales),
+ * 2 = E4M3 kind::f8f6f4 K32.  cycles: device uint64 [2*ctas]; per CTA, SM
+ * clock cycles and then nanoseconds from the first issue to completion of
+ * the last MMA.  Each CTA gets an SM of its own.  Dense
+ * FLOP per SM per cycle = 2*128*256*K*4*iters / cycles.  This is the
+ * "tensor-pipe peak" denominator; the pages publish no rate. */
+int tg_probe_mma_rate(int kind, int iters, int ctas, unsigned long long* cycles,
+                      void* cuda_stream);
+
 /* Waits on an mbarrier that nothing completes, with deadline `timeout_ns`
  * (1..10^9); the bounded wait gives up and records TG_ERR_TIMEOUT with site
  * code 99 in the status word that tg_device_status() returns. */

@@ -143,3 +143,22 @@ def test_bounded_wait_reports_timeout_without_fault(P):
     assert tg.tg_device_status() == (tg.TG_OK, 0)
     x = torch.ones(4, device="cuda")          # the context is still usable
     assert float((x + 1).sum()) == 8.0
+
+
+@pytest.mark.parametrize("kind,k", [(0, 16), (1, 32), (2, 32)])
+def test_mma_rate_probe_runs(P, kind, k):
+    # Back-to-back MMAs on every SM: the measured dense rate per SM and cycle
+    # must be positive and not above the nominal 8192 (bf16) / 16384 (fp8)
+    # FLOP per SM per cycle by more than timing noise.
+    torch = torch_cuda()
+    import blackwell_tile_gemm_gb300 as tg
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = torch.zeros(2 * sms, dtype=torch.int64, device="cuda")
+    iters = 256
+    P.mma_rate(kind, iters, sms, out)
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    cyc = out.cpu().numpy()[0::2].astype(np.float64)
+    assert np.all(cyc > 0)
+    per_clk = 2 * 128 * 256 * k * 4 * iters / cyc
+    nominal = 8192 if kind == 0 else 16384
+    assert per_clk.max() <= 1.05 * nominal
