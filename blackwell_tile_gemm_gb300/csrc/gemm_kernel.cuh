@@ -39,6 +39,7 @@ enum : uint32_t {
   kSiteMmaFull = 2,
   kSiteMmaAccEmpty = 3,
   kSiteEpiAccFull = 4,
+  kSiteScaleFull = 5,
 };
 
 struct GemmArgs {
@@ -81,7 +82,8 @@ struct GemmCfg {
   static constexpr int OFF_SFA = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + kStages * SFA_BYTES;
   static constexpr int OFF_BAR = (OFF_SFB + kStages * SFB_BYTES + 7) & ~7;
-  static constexpr int NUM_BARS = 2 * kStages + 2 * kAccBufs + 1;
+  static constexpr int NUM_BARS =
+      (kMx && kCtaGroup == 2 ? 3 : 2) * kStages + 2 * kAccBufs + (kMx && kCtaGroup == 2 ? 2 : 1);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   // tensor memory columns
@@ -102,7 +104,11 @@ struct GemmCfg {
   static constexpr int kEpiWarps = 8;
   static constexpr int kEpiCols = BN / 2;
   static constexpr int kEpiChunks = kEpiCols / 32;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  // Block-scaled CTA pairs: a separate warp copies the scales into TMEM so
+  // that the copies overlap the MMAs instead of queueing in front of them.
+  static constexpr bool kSfWarp = kMx && kCtaGroup == 2;
+  static constexpr int kSfWarpId = 2 + kEpiWarps;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + (kSfWarp ? 32 : 0);
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N");
@@ -193,6 +199,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t* accf_bar = bars + 2 * C::kStages;         // [kAccBufs] MMA -> epilogue
   uint64_t* acce_bar = accf_bar + C::kAccBufs;        // [kAccBufs] epilogue -> MMA
   uint64_t* drain_bar = acce_bar + C::kAccBufs;       // MMA completion on give-up
+  uint64_t* sfr_bar = drain_bar + 1;                  // [kStages] scales in TMEM -> MMA
+  uint64_t* sf_drain_bar = sfr_bar + C::kStages;      // scale copies on give-up
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -211,6 +219,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&acce_bar[b], C::kEpiWarps * C::kCtaGroup);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (C::kSfWarp) {
+      for (int s = 0; s < C::kStages; ++s) mbar_init(&sfr_bar[s], 1);
+      mbar_init(sf_drain_bar, 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -315,7 +327,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      const uint32_t full0 = smem_addr(&full_bar[0]);
       const uint32_t acce0 = smem_addr(&acce_bar[0]);
       // K-major, 128-byte swizzled operands: 8-row groups 1024 bytes apart;
       // the K16 / K32 slice k of a stage starts 32 * k bytes into each row.
@@ -333,7 +344,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      bool ready = false;       // full barrier of `stage` already seen complete
+      bool ready = false;       // ready barrier of `stage` already seen complete
+      // The MMAs of a stage wait for its TMA data, or with a scale warp for
+      // its scales in TMEM (which that warp copies after the data landed).
+      uint64_t* ready_bar = C::kSfWarp ? sfr_bar : full_bar;
+      const uint32_t ready0 = smem_addr(&ready_bar[0]);
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         if (!mbar_try_wait(acce0 + 8u * acc, acc_phase ^ 1u) &&
             !mbar_wait(&acce_bar[acc], acc_phase ^ 1u, guard, kSiteMmaAccEmpty)) {
@@ -343,8 +358,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!ready && !mbar_try_wait(full0 + 8u * stage, phase) &&
-              !mbar_wait(&full_bar[stage], phase, guard, kSiteMmaFull)) {
+          if (!ready && !mbar_try_wait(ready0 + 8u * stage, phase) &&
+              !mbar_wait(&ready_bar[stage], phase, guard, kSiteMmaFull)) {
             ok = false;
             break;
           }
@@ -354,29 +369,31 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (C::A_BYTES >> 4));
           const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (C::B_BYTES >> 4));
           if constexpr (C::kMx) {
-            // Scales go to this stage's TMEM columns first; the MMAs read them.
             const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_STAGE_COLS;
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-            tmem_cp_32x128b_warpx4<C::kCtaGroup>(
-                sfa_t, sfadesc0 + static_cast<uint64_t>(stage * (C::SFA_BYTES >> 4)));
-#pragma unroll
-            for (int j = 0; j < C::BN / 128; ++j)
+            if constexpr (!C::kSfWarp) {
+              // Scales go to this stage's TMEM columns before the MMAs read them.
               tmem_cp_32x128b_warpx4<C::kCtaGroup>(
-                  sfb_t + 4 * j,
-                  sfbdesc0 + static_cast<uint64_t>(stage * (C::SFB_BYTES >> 4) + 32 * j));
+                  sfa_t, sfadesc0 + static_cast<uint64_t>(stage * (C::SFA_BYTES >> 4)));
+#pragma unroll
+              for (int j = 0; j < C::BN / 128; ++j)
+                tmem_cp_32x128b_warpx4<C::kCtaGroup>(
+                    sfb_t + 4 * j,
+                    sfbdesc0 + static_cast<uint64_t>(stage * (C::SFB_BYTES >> 4) + 32 * j));
+            }
 #pragma unroll
             for (int k = 0; k < C::kIssues; ++k) {
               mma_mxf8<C::kCtaGroup>(d_tmem, ad + 2 * k, bd + 2 * k,
                                      idesc_mxf8_e4m3(C::MMA_M, C::BN, k, k), sfa_t, sfb_t,
                                      (kb | k) != 0);
-              if (k == 0) ready = mbar_try_wait(full0 + 8u * ns, nph);
+              if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           } else {
 #pragma unroll
             for (int k = 0; k < C::kIssues; ++k) {
               mma_bf16<C::kCtaGroup>(d_tmem, ad + 2 * k, bd + 2 * k,
                                      idesc_bf16_f32(C::MMA_M, C::BN), (kb | k) != 0);
-              if (k == 0) ready = mbar_try_wait(full0 + 8u * ns, nph);
+              if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           }
           if constexpr (C::kCtaGroup == 1)
@@ -404,6 +421,51 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         else
           mma_commit_pair(drain_bar, 0x1);
         mbar_wait_drain(drain_bar, 0, p.timeout_ns);
+      }
+    }
+  } else if (C::kSfWarp && warp == C::kSfWarpId) {
+    // ------------------------------------------------------------ scale copier
+    if constexpr (C::kSfWarp) {
+      if (lane == 0 && leader) {
+        const uint64_t sfadesc0 =
+            make_smem_desc(smem_addr(smem + C::OFF_SFA), 16, 128, kDescSwizzleNone);
+        const uint64_t sfbdesc0 =
+            make_smem_desc(smem_addr(smem + C::OFF_SFB), 16, 128, kDescSwizzleNone);
+        const uint32_t full0 = smem_addr(&full_bar[0]);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool copied = false;
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+            if (!mbar_try_wait(full0 + 8u * stage, phase) &&
+                !mbar_wait(&full_bar[stage], phase, guard, kSiteScaleFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            // 32 rows x 16 bytes per copy, 8-row groups 128 bytes apart.
+            const uint32_t tcol = tmem_base + C::SF_COL0 + stage * C::SF_STAGE_COLS;
+            tmem_cp_32x128b_warpx4<C::kCtaGroup>(
+                tcol, sfadesc0 + static_cast<uint64_t>(stage * (C::SFA_BYTES >> 4)));
+#pragma unroll
+            for (int j = 0; j < C::BN / 128; ++j)
+              tmem_cp_32x128b_warpx4<C::kCtaGroup>(
+                  tcol + C::SFA_COLS + 4 * j,
+                  sfbdesc0 + static_cast<uint64_t>(stage * (C::SFB_BYTES >> 4) + 32 * j));
+            mma_commit_pair(&sfr_bar[stage], 0x1);
+            copied = true;
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (copied && (!ok || *abort_flag)) {
+          // Gave up: the copies already issued finish before TMEM is freed.
+          mma_commit_pair(sf_drain_bar, 0x1);
+          mbar_wait_drain(sf_drain_bar, 0, p.timeout_ns);
+        }
       }
     }
   } else {
