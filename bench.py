@@ -40,8 +40,51 @@ from blackwell_tile_gemm_gb300 import synth  # noqa: E402
 METRIC = "GEMM TFLOP/s at 1 GB300 (bf16, MXFP8) and % of dense tensor-pipe peak"
 UNIT = "TFLOP/s"
 SIZE = 8192
-WORKLOAD = ("bf16 GEMM 8192^3 fp32 D (CTA pairs) + MXFP8 GEMM 8192^3 bf16 D (CTA pairs) "
-            "+ b16 transpose 8192^2")
+def workload() -> str:
+    return (f"bf16 GEMM {SIZE}^3 fp32 D (CTA pairs) + MXFP8 GEMM {SIZE}^3 bf16 D (CTA pairs) "
+            f"+ b16 transpose {SIZE}^2")
+
+
+# Per-launch DRAM traffic of each kernel comes from a committed ncu summary
+# under profiles/, valid only while the kernel sources still hash to the
+# value recorded next to the counters (otherwise the traffic is reported as
+# null: the counters describe an older kernel).
+_CSRC = "blackwell_tile_gemm_gb300/csrc/"
+KERNEL_SOURCES = {
+    "gemm": [_CSRC + f for f in ("gemm_kernel.cuh", "tg_ptx.cuh", "gemm_launch.cuh",
+                                 "gemm_bf16.cu", "gemm_mxfp8.cu")],
+    "transpose": [_CSRC + f for f in ("transpose.cu", "tg_ptx.cuh")],
+}
+PROFILES = {
+    "gemm_bf16": ("profiles/gemm_bf16_8192_pair.md", "gemm"),
+    "gemm_mxfp8_blockscaled": ("profiles/gemm_mxfp8_8192_pair.md", "gemm"),
+    "tile_transpose_b16": ("profiles/transpose_b16_8192.md", "transpose"),
+}
+
+
+def sources_sha256(group: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[group]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the kernel's ncu summary, or None if stale/absent."""
+    path, group = PROFILES[kernel]
+    try:
+        with open(os.path.join(ROOT, path)) as fh:
+            fields = dict(line.split(": ", 1) for line in fh.read().splitlines() if ": " in line)
+    except OSError:
+        return None
+    if fields.get("kernel_sources_sha256", "").strip() != sources_sha256(group):
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ---------------------------------------------------------------------------
@@ -137,9 +180,9 @@ def make_step_inputs(torch, dev):
         return torch.from_numpy(bits).to(dev)
 
     host = {
-        "bf16": synth.make_inputs("sq8k"),
-        "mx": synth.make_inputs("mx8k"),
-        "tr": synth.make_inputs("tr8k"),
+        "bf16": synth.make_inputs("sq8k", M=SIZE, N=SIZE, K=SIZE),
+        "mx": synth.make_inputs("mx8k", M=SIZE, N=SIZE, K=SIZE),
+        "tr": synth.make_inputs("tr8k", M=SIZE, N=SIZE),
     }
     d = {
         "A": bf16(host["bf16"]["A"]), "B": bf16(host["bf16"]["B"]),
@@ -250,7 +293,8 @@ def run_ours(args, rank, world, local):
     roofline = {"bound": "hbm" if dominant == "tile_transpose_b16" else "tensor",
                 "kernel": dominant, "achieved": achieved, "peak": peak,
                 "unit": "GB/s" if dominant == "tile_transpose_b16" else "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak,
+                "traffic": profiled_traffic(dominant) if SIZE == 8192 else None,
                 "peak_source": peak_note}
 
     e2e = measure_e2e(torch, tg, host, dev, stream, args.e2e_steps if args.kernel == "all" else 0,
@@ -263,7 +307,7 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3 (f32 accumulate)",
         "data": "synthetic (seeded numpy; recipes in blackwell_tile_gemm_gb300/synth.py)",
-        "config": {"workload": WORKLOAD if args.kernel == "all" else f"{args.kernel} only",
+        "config": {"workload": workload() if args.kernel == "all" else f"{args.kernel} only",
                    "M": SIZE, "N": SIZE, "K": SIZE,
                    "tiles": "256x256 per CTA pair, 128-byte K stages",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -337,8 +381,8 @@ _SAMPLE = {}
 
 def _oracle_sample_inputs():
     if not _SAMPLE:
-        _SAMPLE["bf16"] = synth.make_inputs("sq8k")
-        _SAMPLE["mx"] = synth.make_inputs("mx8k")
+        _SAMPLE["bf16"] = synth.make_inputs("sq8k", M=SIZE, N=SIZE, K=SIZE)
+        _SAMPLE["mx"] = synth.make_inputs("mx8k", M=SIZE, N=SIZE, K=SIZE)
     return _SAMPLE
 
 
@@ -358,19 +402,21 @@ def oracle_sample(rows_per_gemm: int, cols: int, offset: int):
 
 
 def cpu_baseline(target_seconds: float):
+    """The oracle on a growing sample until one run takes about target_seconds."""
     import oracle
     oracle.build()
     _oracle_sample_inputs()
     cores = oracle.num_threads()
+    cols = min(1024, SIZE)
     rows = max(cores, 16)
-    flops, dt = oracle_sample(rows, 1024, 0)            # calibration
-    scale = max(1.0, target_seconds / max(dt, 1e-3))
-    rows = int(rows * scale)
-    flops, dt = oracle_sample(rows, 1024, 1)
+    flops, dt = oracle_sample(rows, cols, 0)
+    while dt < 0.6 * target_seconds and rows < SIZE:
+        rows = min(SIZE, rows * 2)
+        flops, dt = oracle_sample(rows, cols, rows)
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "seconds": dt,
-            "sample": (f"float64 oracle on {rows} rows x 1024 columns (all K = 8192) of each "
-                       f"8192^3 GEMM (bf16 and MXFP8), operands decoded per call")}
+            "sample": (f"float64 oracle on {rows} rows x {cols} columns (all K = {SIZE}) of each "
+                       f"{SIZE}^3 GEMM (bf16 and MXFP8), operands decoded per call")}
 
 
 def run_reference(args, rank, world):
@@ -380,7 +426,7 @@ def run_reference(args, rank, world):
     oracle.build()
     _oracle_sample_inputs()
     cores = oracle.num_threads()
-    rows, cols = cores, 256
+    rows, cols = min(4 * cores, SIZE), min(512, SIZE)
     for _ in range(args.warmup):
         oracle_sample(rows, cols, 0)
     flops = 0.0
@@ -390,14 +436,14 @@ def run_reference(args, rank, world):
         flops += f
         secs += dt
     value = flops / secs / 1e12
-    sample = (f"per step: float64 oracle on {rows} rows x {cols} columns (all K = 8192) of "
-              f"each 8192^3 GEMM (bf16 and MXFP8)")
+    sample = (f"per step: float64 oracle on {rows} rows x {cols} columns (all K = {SIZE}) of "
+              f"each {SIZE}^3 GEMM (bf16 and MXFP8)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded numpy; recipes in blackwell_tile_gemm_gb300/synth.py)",
-        "config": {"workload": WORKLOAD if args.kernel == "all" else f"{args.kernel} only",
+        "config": {"workload": workload() if args.kernel == "all" else f"{args.kernel} only",
                    "M": SIZE, "N": SIZE, "K": SIZE,
                    "parallelism": "host cores (OpenMP over output rows)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -451,11 +497,17 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--size", type=int, default=8192,
+                    help="M = N = K of the GEMMs and the transpose side (default 8192)")
     ap.add_argument("--kernel", choices=["all", "gemm_bf16", "gemm_mxfp8", "transpose"],
                     default="all", help="run one part of the step only (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.size < 256 or args.size % 256:
+        ap.error("--size must be a positive multiple of 256")
+    global SIZE
+    SIZE = args.size
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
