@@ -373,6 +373,62 @@ def measure_e2e(torch, tg, host, dev, stream, steps, flops_step):
 
 
 # ---------------------------------------------------------------------------
+# per-workload table (--configs): one JSON line per workload, not the contract line
+# ---------------------------------------------------------------------------
+
+def run_configs(args):
+    import torch
+
+    import blackwell_tile_gemm_gb300 as tg
+    from blackwell_tile_gemm_gb300 import build as tgbuild
+
+    tgbuild.build()
+    dev = torch.device("cuda", 0)
+    peaks, _ = measured_peaks()
+    for name, w in synth.WORKLOADS.items():
+        x = synth.make_inputs(w)
+        if w.kind == "transpose":
+            X = torch.from_numpy(x["X"].view(np.int16)).to(dev)
+            out = torch.empty((w.N, w.M), dtype=torch.int16, device=dev)
+            fn = lambda: tg.tile_transpose_b16(X, out)           # noqa: E731
+        elif w.kind == "mxfp8":
+            A, B, SFA, SFB = (torch.from_numpy(x[k]).to(dev) for k in ("A", "B", "SFA", "SFB"))
+            D = torch.empty((w.M, w.N), device=dev,
+                            dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
+            fn = lambda: tg.gemm_mxfp8_blockscaled(A, B, SFA, SFB, D, cta_pair=w.cta_pair)  # noqa
+        else:
+            A = torch.from_numpy(x["A"].view(np.int16)).to(dev).view(torch.bfloat16)
+            B = torch.from_numpy(x["B"].view(np.int16)).to(dev).view(torch.bfloat16)
+            D = torch.empty((w.M, w.N), device=dev,
+                            dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
+            add = w.epi_add if w.epi_add else None
+            fn = lambda: tg.gemm_bf16(A, B, D, epilogue_add=add, cta_pair=w.cta_pair)  # noqa
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(20):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        code, _ = tg.tg_device_status()
+        ms = statistics.median(times)
+        line = {"workload": name, "describe": w.describe, "status": code, "ms_median": ms}
+        if w.kind == "transpose":
+            gbs = 2 * 2 * w.M * w.N / (ms * 1e-3) / 1e9
+            line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]))
+        else:
+            tf = w.flops / (ms * 1e-3) / 1e12
+            pk = float(peaks["bf16_tflops"]) * (2 if w.kind == "mxfp8" else 1)
+            line.update(tflops=tf, frac_of_cublas_bf16_burst_scaled=tf / pk)
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
 
@@ -497,6 +553,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--configs", action="store_true",
+                    help="time every workload of the table (one JSON line each) and exit")
     ap.add_argument("--size", type=int, default=8192,
                     help="M = N = K of the GEMMs and the transpose side (default 8192)")
     ap.add_argument("--kernel", choices=["all", "gemm_bf16", "gemm_mxfp8", "transpose"],
@@ -509,6 +567,9 @@ def main(argv=None):
     global SIZE
     SIZE = args.size
     rank, world, local = dist_env()
+    if args.configs:
+        run_configs(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

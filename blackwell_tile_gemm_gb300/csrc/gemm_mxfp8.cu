@@ -38,34 +38,45 @@ struct SfImage {
   uint32_t* dst;        // [num_kg][blocks][128] words
 };
 
-// One thread per 32-bit word of the images: word (4*l + j) of block b, K group
-// g holds the scales of row 128*b + 32*j + l for K blocks 4*g .. 4*g+3 (low
-// byte first).  Rows or blocks past the end are zero.
+// Image word (4*l + j) of 128-row block b, K group g holds the scales of row
+// 128*b + 32*j + l for K blocks 4*g .. 4*g+3 (low byte first); rows or K
+// blocks past the end are zero.  Work unit: one warp per (image, block,
+// quad of K groups, l-octet).  Lane (4*l' + j) reads the 16 scale bytes of
+// K groups 4*quad .. 4*quad+3 of its row and writes one word into each of
+// those four images, so that each warp store covers 32 consecutive words
+// (128 bytes) of one image.
 __global__ void sf_repack_kernel(SfImage a, SfImage b, int kblocks, int num_kg) {
-  const int64_t words_a = static_cast<int64_t>(num_kg) * a.blocks * 128;
-  const int64_t words_b = static_cast<int64_t>(num_kg) * b.blocks * 128;
-  for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-       w < words_a + words_b; w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const bool is_a = w < words_a;
+  const int quads = (num_kg + 3) / 4;
+  const int64_t warps_a = static_cast<int64_t>(a.blocks) * quads * 4;
+  const int64_t warps_b = static_cast<int64_t>(b.blocks) * quads * 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_per_grid = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t wid = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
+       wid < warps_a + warps_b; wid += warps_per_grid) {
+    const bool is_a = wid < warps_a;
     const SfImage& s = is_a ? a : b;
-    const int64_t ww = is_a ? w : w - words_a;
-    const int64_t per_kg = static_cast<int64_t>(s.blocks) * 128;
-    const int kg = static_cast<int>(ww / per_kg);
-    const int rem = static_cast<int>(ww - kg * per_kg);
-    const int blk = rem >> 7;
-    const int lw = rem & 127;
-    const int l = lw >> 2, j = lw & 3;
-    const int row = blk * 128 + j * 32 + l;
-    uint32_t v = 0;
+    const int64_t w = is_a ? wid : wid - warps_a;
+    const int octet = static_cast<int>(w & 3);
+    const int64_t bq = w >> 2;
+    const int quad = static_cast<int>(bq % quads);
+    const int blk = static_cast<int>(bq / quads);
+    const int l = 8 * octet + (lane >> 2), j = lane & 3;
+    const int row = blk * 128 + 32 * j + l;
+    uint32_t v[4] = {0, 0, 0, 0};
     if (row < s.rows) {
       const uint8_t* src = s.src + static_cast<int64_t>(row) * s.ld;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int kb = kg * 4 + k;
-        if (kb < kblocks) v |= static_cast<uint32_t>(src[kb]) << (8 * k);
+      for (int t = 0; t < 16; ++t) {
+        const int kb = 16 * quad + t;
+        if (kb < kblocks) v[t >> 2] |= static_cast<uint32_t>(__ldg(src + kb)) << (8 * (t & 3));
       }
     }
-    s.dst[ww] = v;
+    const int64_t per_kg = static_cast<int64_t>(s.blocks) * 128;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int kg = 4 * quad + t;
+      if (kg < num_kg) s.dst[kg * per_kg + blk * 128 + 4 * l + j] = v[t];
+    }
   }
 }
 
@@ -105,9 +116,10 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
              reinterpret_cast<uint32_t*>(img_a)};
   SfImage sb{static_cast<const uint8_t*>(SFB), ld_sfb, N, pl.sfb_blocks,
              reinterpret_cast<uint32_t*>(img_b)};
-  const int64_t words = static_cast<int64_t>(pl.num_kg) * (pl.sfa_blocks + pl.sfb_blocks) * 128;
-  int64_t blocks = (words + 255) / 256;
-  if (blocks > 8 * static_cast<int64_t>(ctx->num_sms)) blocks = 8 * ctx->num_sms;
+  const int64_t warps =
+      static_cast<int64_t>((pl.num_kg + 3) / 4) * (pl.sfa_blocks + pl.sfb_blocks) * 4;
+  int64_t blocks = (warps + 7) / 8;
+  if (blocks > 16 * static_cast<int64_t>(ctx->num_sms)) blocks = 16 * ctx->num_sms;
   sf_repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(sa, sb, K / 32, pl.num_kg);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
