@@ -34,6 +34,7 @@ TG_D_BF16 = 1
 TG_EPI_NONE = 0
 TG_EPI_ADD_SCALAR = 1
 TG_FLAG_CTA_PAIR = 1
+TG_FLAG_MULTICAST = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -128,12 +129,20 @@ def _d_code(dtype):
     raise ValueError(f"D must be float32 or bfloat16, got {dtype}")
 
 
-def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, cta_pair=False, stream=None):
+def _flags(cta_pair, multicast):
+    if multicast and not cta_pair:
+        raise ValueError("multicast needs cta_pair=True")
+    return (TG_FLAG_CTA_PAIR if cta_pair else 0) | (TG_FLAG_MULTICAST if multicast else 0)
+
+
+def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, cta_pair=False,
+              multicast=False, stream=None):
     """D[M,N] = A[M,K] @ B[N,K].T (+ epilogue_add), bf16 inputs, f32 accumulation.
 
     A, B: CUDA bfloat16 tensors with unit inner stride.  D: optional output
     (float32 or bfloat16, [M, N]); otherwise allocated with ``out_dtype``
-    (default float32).  ``cta_pair`` selects the two-CTA (cta_group::2) kernel.
+    (default float32).  ``cta_pair`` selects the two-CTA (cta_group::2) kernel;
+    ``multicast`` (with ``cta_pair``) runs clusters of two pairs sharing B.
     """
     import torch
     M, K = A.shape
@@ -149,14 +158,14 @@ def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, cta_pair=False
     epi = TG_EPI_NONE if epilogue_add is None else TG_EPI_ADD_SCALAR
     rc = lib().gemm_bf16(A.data_ptr(), _ld(A, "A", 8), B.data_ptr(), _ld(B, "B", 8),
                          D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
-                         float(epilogue_add or 0.0), TG_FLAG_CTA_PAIR if cta_pair else 0,
+                         float(epilogue_add or 0.0), _flags(cta_pair, multicast),
                          _stream_handle(stream))
     _check(rc, "gemm_bf16")
     return D
 
 
 def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_add=None,
-                           cta_pair=False, stream=None):
+                           cta_pair=False, multicast=False, stream=None):
     """Block-scaled MXFP8 product: D = (A * 2^(SFA-127)) @ (B * 2^(SFB-127)).T.
 
     A: [M, K], B: [N, K] E4M3FN bytes (torch.float8_e4m3fn or uint8); SFA:
@@ -182,13 +191,13 @@ def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_a
         A.data_ptr(), _ld(A, "A", 16), B.data_ptr(), _ld(B, "B", 16),
         SFA.data_ptr(), _ld(SFA, "SFA", 1), SFB.data_ptr(), _ld(SFB, "SFB", 1),
         D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
-        float(epilogue_add or 0.0), TG_FLAG_CTA_PAIR if cta_pair else 0, _stream_handle(stream))
+        float(epilogue_add or 0.0), _flags(cta_pair, multicast), _stream_handle(stream))
     _check(rc, "gemm_mxfp8_blockscaled")
     return D
 
 
 def gemm_mxfp8_blockscaled_noalloc(A, B, SFA, SFB, D, *, epilogue_add=None, cta_pair=False,
-                                   stream=None):
+                                   multicast=False, stream=None):
     """``gemm_mxfp8_blockscaled`` for callers that must not allocate device memory.
 
     Same arguments and result, except that D must be supplied (this call
@@ -206,7 +215,7 @@ def gemm_mxfp8_blockscaled_noalloc(A, B, SFA, SFB, D, *, epilogue_add=None, cta_
         A.data_ptr(), _ld(A, "A", 16), B.data_ptr(), _ld(B, "B", 16),
         SFA.data_ptr(), _ld(SFA, "SFA", 1), SFB.data_ptr(), _ld(SFB, "SFB", 1),
         D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
-        float(epilogue_add or 0.0), TG_FLAG_CTA_PAIR if cta_pair else 0, _stream_handle(stream))
+        float(epilogue_add or 0.0), _flags(cta_pair, multicast), _stream_handle(stream))
     _check(rc, "gemm_mxfp8_blockscaled_noalloc")
     return D
 

@@ -149,15 +149,16 @@ int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
   if (K == 0)
     return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi_add ? epi_scalar : 0.0f, stream);
   const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
+  const bool mcast = (flags & TG_FLAG_MULTICAST) != 0;
   if (!mx)
     return launch_gemm_bf16_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M),
                                  static_cast<int>(N), static_cast<int>(K), d_dtype, epi_add,
-                                 epi_scalar, pair, stream, ctx);
+                                 epi_scalar, pair, mcast, stream, ctx);
   uint8_t* ws = static_cast<uint8_t*>(device_workspace(mxfp8_workspace_bytes(M, N, K, pair)));
   if (ws == nullptr) return TG_ERR_CUDA;
   return launch_gemm_mxfp8_impl(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
                                 static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                d_dtype, epi_add, epi_scalar, pair, ws, stream, ctx);
+                                d_dtype, epi_add, epi_scalar, pair, mcast, ws, stream, ctx);
 }
 
 }  // namespace tg
@@ -175,7 +176,9 @@ int check_gemm_common(const void* A, int64_t lda, const void* B, int64_t ldb, vo
     return TG_ERR_INVALID_ARG;
   if (d_dtype != TG_D_F32 && d_dtype != TG_D_BF16) return TG_ERR_INVALID_ARG;
   if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_ADD_SCALAR) return TG_ERR_INVALID_ARG;
-  if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR)) return TG_ERR_UNSUPPORTED;
+  if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST))
+    return TG_ERR_UNSUPPORTED;
+  if ((flags & TG_FLAG_MULTICAST) && !(flags & TG_FLAG_CTA_PAIR)) return TG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TG_OK;
   if (D == nullptr || ldd < N) return TG_ERR_INVALID_ARG;
   const int d_esize = d_dtype == TG_D_F32 ? 4 : 2;

@@ -5,6 +5,9 @@
 //   CTA pair   : 256 x 256 tiles per cluster of two (cta_group::2), each CTA
 //                stages 128 rows of A and 128 rows of B per stage (32 KB),
 //                6-stage ring, two accumulators per CTA.
+//   multicast  : clusters of two CTA pairs on vertically adjacent tiles; each
+//                CTA loads a 64-row quarter of the shared B tile and
+//                multicasts it to its counterpart in the other pair.
 #include "gemm_launch.cuh"
 
 namespace tg {
@@ -16,11 +19,15 @@ using CfgF32 = GemmCfg<1, false, 256, 2, 4, false>;
 using CfgBf16 = GemmCfg<1, false, 256, 2, 4, true>;
 using CfgPairF32 = GemmCfg<2, false, 256, 2, 6, false>;
 using CfgPairBf16 = GemmCfg<2, false, 256, 2, 6, true>;
+// Clusters of two CTA pairs multicasting the shared B tile (TG_FLAG_MULTICAST).
+using CfgPairMcF32 = GemmCfg<2, false, 256, 2, 6, false, true>;
+using CfgPairMcBf16 = GemmCfg<2, false, 256, 2, 6, true, true>;
 }  // namespace
 
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
                           int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                          float epi_scalar, bool pair, cudaStream_t stream, DeviceCtx* ctx) {
+                          float epi_scalar, bool pair, bool mcast, cudaStream_t stream,
+                          DeviceCtx* ctx) {
   constexpr int BN = 256;
   const int g = pair ? 2 : 1;
   const int b_rows = BN / g;
@@ -28,7 +35,8 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
   int rc = make_tensor_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, lda * 2, 64, 128,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != TG_OK) return rc;
-  rc = make_tensor_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, ldb * 2, 64, b_rows,
+  const int b_box = pair && mcast ? b_rows / 2 : b_rows;
+  rc = make_tensor_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, ldb * 2, 64, b_box,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != TG_OK) return rc;
   GemmArgs a{};
@@ -49,6 +57,9 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
   if (!pair)
     return bf16_out ? launch_gemm_cfg<CfgBf16>(tA, tB, tA, tB, a, stream, ctx)
                     : launch_gemm_cfg<CfgF32>(tA, tB, tA, tB, a, stream, ctx);
+  if (mcast)
+    return bf16_out ? launch_gemm_cfg<CfgPairMcBf16>(tA, tB, tA, tB, a, stream, ctx)
+                    : launch_gemm_cfg<CfgPairMcF32>(tA, tB, tA, tB, a, stream, ctx);
   return bf16_out ? launch_gemm_cfg<CfgPairBf16>(tA, tB, tA, tB, a, stream, ctx)
                   : launch_gemm_cfg<CfgPairF32>(tA, tB, tA, tB, a, stream, ctx);
 }

@@ -58,9 +58,16 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-template <int kCtaGroup_, bool kMx_, int kBN_, int kAccBufs_, int kStages_, bool kBf16Out_>
+template <int kCtaGroup_, bool kMx_, int kBN_, int kAccBufs_, int kStages_, bool kBf16Out_,
+          bool kMcast_ = false>
 struct GemmCfg {
   static constexpr int kCtaGroup = kCtaGroup_;
+  // Multicast: clusters of two CTA pairs that work on vertically adjacent
+  // tiles share the B tile; each CTA loads a quarter of it and multicasts
+  // the quarter to its counterpart in the other pair.
+  static constexpr bool kMcast = kMcast_;
+  static constexpr int kPairs = kMcast ? 2 : 1;           // MMA units per cluster
+  static constexpr int kClusterCtas = kCtaGroup * kPairs;
   static constexpr bool kMx = kMx_;
   static constexpr int BM = 128;                    // D rows per CTA (TMEM lanes)
   static constexpr int BN = kBN_;                   // D columns per tile (MMA N)
@@ -71,6 +78,7 @@ struct GemmCfg {
   static constexpr int UMMA_K = kMx ? 32 : 16;      // K elements per MMA issue = 32 bytes
   static constexpr int kIssues = BK / UMMA_K;       // 4 issues per stage
   static constexpr int B_ROWS = BN / kCtaGroup;     // B rows this CTA stages
+  static constexpr int B_LOAD_ROWS = B_ROWS / kPairs;  // B rows this CTA loads
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int SFA_BYTES = kMx ? 512 : 0;   // 128 rows x 4 K-blocks
@@ -113,6 +121,7 @@ struct GemmCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
+  static_assert(!kMcast || kCtaGroup == 2, "multicast clusters are made of CTA pairs");
 };
 
 // Grouped tile order: consecutive tile ids walk down a band of `group`
@@ -207,12 +216,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t rank = (C::kCtaGroup == 2) ? cluster_ctarank() : 0u;
-  const bool leader = rank == 0;
+  const uint32_t pair_rank = rank & 1u;               // 0: MMA-issuing CTA of the pair
+  const uint32_t pair_id = rank >> 1;                 // which pair of the cluster
+  const uint32_t lead_rank = rank & ~1u;              // rank of this pair's leader
+  const bool leader = pair_rank == 0;
+  // tcgen05.commit multicast masks: this pair, and every CTA whose loads
+  // land in this pair's shared memory (both pairs under multicast).
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << lead_rank);
+  const uint16_t stage_mask = C::kMcast ? static_cast<uint16_t>(0xF) : pair_mask;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], C::kPairs);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&accf_bar[b], 1);
@@ -245,9 +261,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitGuard guard{p.status, abort_flag, p.timeout_ns};
-  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
-  const int unit = blockIdx.x / C::kCtaGroup;         // CTA or CTA pair index
-  const int num_units = gridDim.x / C::kCtaGroup;
+  // Work units: tiles of kPairs x 256 rows (one per cluster) by BN columns.
+  const int num_mc = (p.num_m_tiles + C::kPairs - 1) / C::kPairs;
+  const int num_tiles = num_mc * p.num_n_tiles;
+  const int unit = blockIdx.x / C::kClusterCtas;      // cluster index
+  const int num_units = gridDim.x / C::kClusterCtas;
 
   // The producer and MMA loops run one thread each and are latency-critical:
   // the tensor pipe queues only a couple of MMAs, so every instruction the
@@ -267,17 +285,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t empty0 = smem_addr(&empty_bar[0]);
       const uint32_t full0 = smem_addr(&full_bar[0]);
       // Pair: both CTAs' loads complete on the leader's barrier.
-      const uint32_t full_dst0 = C::kCtaGroup == 2 ? map_to_cta(full0, 0) : full0;
+      const uint32_t full_dst0 = C::kCtaGroup == 2 ? map_to_cta(full0, lead_rank) : full0;
+      const uint16_t mcast_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2u)));
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;   // per-stage bit masks
       bool ok = true;
       for (int t = unit; t < num_tiles && ok; t += num_units) {
-        int tm, tn;
-        tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.raster_group, tm, tn);
-        const int a_row = tm * C::MMA_M + static_cast<int>(rank) * C::BM;
-        const int b_row = tn * C::BN + static_cast<int>(rank) * C::B_ROWS;
-        const int sfa_row = C::kCtaGroup == 2 ? tm * 2 + static_cast<int>(rank) : tm;
+        int tmc, tn;
+        tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
+        const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
+        const int a_row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM;
+        const int b_row = tn * C::BN + static_cast<int>(pair_rank) * C::B_ROWS;
+        const int sfa_row = C::kCtaGroup == 2 ? tm * 2 + static_cast<int>(pair_rank) : tm;
         const int sfb_row = tn * (C::BN / 128);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_try_wait(empty0 + 8u * stage, phase ^ 1u) &&
@@ -301,7 +321,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             // Only the leader posts the expected byte count (for the pair).
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_TX);
             tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, fb, kx, a_row, pol_ab);
-            tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+            if constexpr (C::kMcast) {
+              // This CTA's quarter of the B tile, into itself and its
+              // counterpart in the other pair (same offset in both).
+              tma_load_2d_pair_mcast(
+                  sB + stage * C::B_BYTES + pair_id * (C::B_LOAD_ROWS * 128), &tmB, fb, kx,
+                  b_row + static_cast<int>(pair_id) * C::B_LOAD_ROWS, mcast_mask, pol_ab);
+            } else {
+              tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+            }
             if constexpr (C::kMx) {
               tma_load_2d_pair(sSFA + stage * C::SFA_BYTES, &tmSFA, fb, 0,
                                kb * p.sfa_blocks + sfa_row, pol_ab);
@@ -399,7 +427,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if constexpr (C::kCtaGroup == 1)
             mma_commit(&empty_bar[stage]);
           else
-            mma_commit_pair(&empty_bar[stage], 0x3);
+            mma_commit_pair(&empty_bar[stage], stage_mask);
           stage = ns;
           phase = nph;
         }
@@ -407,7 +435,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if constexpr (C::kCtaGroup == 1)
           mma_commit(&accf_bar[acc]);
         else
-          mma_commit_pair(&accf_bar[acc], 0x3);
+          mma_commit_pair(&accf_bar[acc], pair_mask);
         if (++acc == C::kAccBufs) {
           acc = 0;
           acc_phase ^= 1u;
@@ -419,7 +447,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if constexpr (C::kCtaGroup == 1)
           mma_commit(drain_bar);
         else
-          mma_commit_pair(drain_bar, 0x1);
+          mma_commit_pair(drain_bar, static_cast<uint16_t>(1u << lead_rank));
         mbar_wait_drain(drain_bar, 0, p.timeout_ns);
       }
     }
@@ -453,7 +481,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               tmem_cp_32x128b_warpx4<C::kCtaGroup>(
                   tcol + C::SFA_COLS + 4 * j,
                   sfbdesc0 + static_cast<uint64_t>(stage * (C::SFB_BYTES >> 4) + 32 * j));
-            mma_commit_pair(&sfr_bar[stage], 0x1);
+            mma_commit_pair(&sfr_bar[stage], static_cast<uint16_t>(1u << lead_rank));
             copied = true;
             if (++stage == C::kStages) {
               stage = 0;
@@ -463,7 +491,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         if (copied && (!ok || *abort_flag)) {
           // Gave up: the copies already issued finish before TMEM is freed.
-          mma_commit_pair(sf_drain_bar, 0x1);
+          mma_commit_pair(sf_drain_bar, static_cast<uint16_t>(1u << lead_rank));
           mbar_wait_drain(sf_drain_bar, 0, p.timeout_ns);
         }
       }
@@ -477,10 +505,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t acce_remote = 0;
-    if constexpr (C::kCtaGroup == 2) acce_remote = map_to_cta(smem_addr(&acce_bar[0]), 0);
+    if constexpr (C::kCtaGroup == 2) acce_remote = map_to_cta(smem_addr(&acce_bar[0]), lead_rank);
     for (int t = unit; t < num_tiles; t += num_units) {
-      int tm, tn;
-      tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.raster_group, tm, tn);
+      int tmc, tn;
+      tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
+      const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
       // One lane waits for the accumulator; the others wait at the warp barrier.
       int got = 1;
       if (lane == 0) got = mbar_wait(&accf_bar[acc], acc_phase, guard, kSiteEpiAccFull) ? 1 : 0;
@@ -503,7 +532,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         else
           mbar_arrive_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
       }
-      const int row = tm * C::MMA_M + static_cast<int>(rank) * C::BM + row_in_tile;
+      const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
 #pragma unroll
       for (int c = 0; c < C::kEpiChunks; ++c) {
         const int col0 = tn * C::BN + half * C::kEpiCols + 32 * c;

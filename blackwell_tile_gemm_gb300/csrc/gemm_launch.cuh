@@ -28,15 +28,15 @@ int gemm_units_for_device(DeviceCtx* ctx) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return -cuda_fail(e);
-  int units = ctx->num_sms / C::kCtaGroup;
+  int units = ctx->num_sms / C::kClusterCtas;
   if constexpr (C::kCtaGroup == 2) {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = C::kClusterCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(C::kClusterCtas * units), 1, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.attrs = attr;
@@ -57,17 +57,17 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
                     DeviceCtx* ctx) {
   const int units_max = gemm_units_for_device<C>(ctx);
   if (units_max < 0) return TG_ERR_CUDA;
-  const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+  const int num_tiles = (args.num_m_tiles + C::kPairs - 1) / C::kPairs * args.num_n_tiles;
   const int units = num_tiles < units_max ? num_tiles : units_max;
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(static_cast<unsigned>(units * C::kCtaGroup), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(units * C::kClusterCtas), 1, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   if constexpr (C::kCtaGroup == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = C::kClusterCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

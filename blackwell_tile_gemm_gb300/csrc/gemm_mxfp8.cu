@@ -29,6 +29,8 @@ using CfgMxF32 = GemmCfg<1, true, 256, 1, 4, false>;
 using CfgMxBf16 = GemmCfg<1, true, 256, 1, 4, true>;
 using CfgMxPairF32 = GemmCfg<2, true, 256, 1, 6, false>;
 using CfgMxPairBf16 = GemmCfg<2, true, 256, 1, 6, true>;
+using CfgMxPairMcF32 = GemmCfg<2, true, 256, 1, 6, false, true>;
+using CfgMxPairMcBf16 = GemmCfg<2, true, 256, 1, 6, true, true>;
 
 struct SfImage {
   const uint8_t* src;   // [rows, kblocks] bytes, row stride ld
@@ -105,7 +107,7 @@ size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair) {
 int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                           float epi_scalar, bool pair, uint8_t* sf_workspace,
+                           float epi_scalar, bool pair, bool mcast, uint8_t* sf_workspace,
                            cudaStream_t stream, DeviceCtx* ctx) {
   const MxPlan pl = plan_mx(M, N, K, pair);
   const int g = pair ? 2 : 1;
@@ -128,8 +130,8 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
   int rc = make_tensor_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, 128,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != TG_OK) return rc;
-  rc = make_tensor_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, ldb, 128, 256 / g,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
+  rc = make_tensor_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, ldb, 128,
+                          pair && mcast ? 256 / g / 2 : 256 / g, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != TG_OK) return rc;
   rc = make_tensor_map_2d(&tSA, CU_TENSOR_MAP_DATA_TYPE_UINT32, img_a, 128,
                           static_cast<uint64_t>(pl.num_kg) * pl.sfa_blocks, 512, 128, 1,
@@ -160,6 +162,9 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
   if (!pair)
     return bf16_out ? launch_gemm_cfg<CfgMxBf16>(tA, tB, tSA, tSB, a, stream, ctx)
                     : launch_gemm_cfg<CfgMxF32>(tA, tB, tSA, tSB, a, stream, ctx);
+  if (mcast)
+    return bf16_out ? launch_gemm_cfg<CfgMxPairMcBf16>(tA, tB, tSA, tSB, a, stream, ctx)
+                    : launch_gemm_cfg<CfgMxPairMcF32>(tA, tB, tSA, tSB, a, stream, ctx);
   return bf16_out ? launch_gemm_cfg<CfgMxPairBf16>(tA, tB, tSA, tSB, a, stream, ctx)
                   : launch_gemm_cfg<CfgMxPairF32>(tA, tB, tSA, tSB, a, stream, ctx);
 }

@@ -98,5 +98,6 @@ extern "C" int gemm_mxfp8_blockscaled_noalloc(const void* A, int64_t lda, const 
   if (scratch == nullptr) return rc;
   return launch_gemm_mxfp8_impl(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
                                 static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                d_dtype, epi_add, epi_scalar, pair, scratch, stream, ctx);
+                                d_dtype, epi_add, epi_scalar, pair,
+                                (flags & TG_FLAG_MULTICAST) != 0, scratch, stream, ctx);
 }

@@ -45,12 +45,13 @@ int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
 
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
                           int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                          float epi_scalar, bool pair, cudaStream_t stream, DeviceCtx* ctx);
+                          float epi_scalar, bool pair, bool mcast, cudaStream_t stream,
+                          DeviceCtx* ctx);
 
 int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                           float epi_scalar, bool pair, uint8_t* sf_workspace,
+                           float epi_scalar, bool pair, bool mcast, uint8_t* sf_workspace,
                            cudaStream_t stream, DeviceCtx* ctx);
 
 // Host-side argument checks of the block-scaled call (no CUDA calls).
@@ -59,7 +60,8 @@ int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb, con
                      int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
                      unsigned flags);
 
-// Bytes of scale-image workspace the MXFP8 path needs for this problem.
+// Bytes of scale-image workspace the MXFP8 path needs for this problem
+// (CTA pairs and multicast clusters share one image layout).
 size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair);
 
 // D = epilogue(0) when K == 0.

@@ -227,6 +227,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// CTA-pair load multicast to the CTAs in `cta_mask` (same shared-memory
+// offset in each); each destination's bytes complete on the barrier at
+// `bar`'s offset in the leader CTA of that destination's pair (`bar` is a
+// pair-leader shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair_mcast(uint32_t dst, const CUtensorMap* map,
+                                                       uint32_t bar, int32_t x, int32_t y,
+                                                       uint16_t cta_mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes.multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask),
+      "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled store shared -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y) {

@@ -64,8 +64,13 @@ enum { TG_EPI_NONE = 0, TG_EPI_ADD_SCALAR = 1 };
 
 /* Launch flags (bit set). */
 enum {
-  TG_FLAG_CTA_PAIR = 1u /* cta_group::2: two CTAs of a cluster share one
-                           256-row MMA; each loads half of the B tile */
+  TG_FLAG_CTA_PAIR = 1u, /* cta_group::2: two CTAs of a cluster share one
+                            256-row MMA; each loads half of the B tile      */
+  TG_FLAG_MULTICAST = 2u /* with TG_FLAG_CTA_PAIR only: clusters of two pairs
+                            on vertically adjacent tiles share the B tile by
+                            TMA multicast (each CTA loads a quarter).  Same
+                            results; on GB300 measured 2-3% slower than plain
+                            pairs at 8192^3, so it is off by default.       */
 };
 
 /*
@@ -78,7 +83,8 @@ enum {
  *          K == 0: D = epilogue(0).  Any size need not be a tile multiple:
  *          loads past the edge read zeros [TMA], stores past it are dropped.
  *   epilogue, epi_scalar: TG_EPI_NONE or TG_EPI_ADD_SCALAR with constant s.
- *   flags: 0 or TG_FLAG_CTA_PAIR.
+ *   flags: 0, TG_FLAG_CTA_PAIR, or TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST
+ *          (TG_FLAG_MULTICAST alone: TG_ERR_INVALID_ARG).
  * Rounding: f32 -> bf16 D is round-to-nearest-even.  Alignment: A, B, D
  * 16-byte aligned; lda*2, ldb*2, ldd*sizeof(D) multiples of 16.
  * Returns TG_OK once the kernel is enqueued, else an error (nothing enqueued).

@@ -58,6 +58,7 @@ A16 = 0x10000           # a 16-byte aligned fake device address (never dereferen
     (dict(d_dtype=7), tg.TG_ERR_INVALID_ARG),
     (dict(epilogue=9), tg.TG_ERR_INVALID_ARG),
     (dict(flags=0x80), tg.TG_ERR_UNSUPPORTED),
+    (dict(flags=2), tg.TG_ERR_INVALID_ARG),         # multicast without CTA pairs
     (dict(A=0), tg.TG_ERR_INVALID_ARG),
     (dict(D=0), tg.TG_ERR_INVALID_ARG),
     (dict(lda=32), tg.TG_ERR_INVALID_ARG),          # lda < K

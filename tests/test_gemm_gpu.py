@@ -24,6 +24,8 @@ def tg():
     return m
 
 
+# `pair`: False = single CTA, True = CTA pair, "mc" = clusters of two pairs
+# sharing the B tile by multicast.
 def run_bf16(tg, A, B, out_dtype="f32", add=None, pair=False, ld_pad=0):
     torch = torch_cuda()
     M, K = A.shape
@@ -34,7 +36,8 @@ def run_bf16(tg, A, B, out_dtype="f32", add=None, pair=False, ld_pad=0):
         D = Dfull[:, :N]
     else:
         D = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
-    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), D, epilogue_add=add, cta_pair=pair)
+    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), D, epilogue_add=add, cta_pair=bool(pair),
+                 multicast=pair == "mc")
     assert tg.tg_device_status()[0] == tg.TG_OK
     return D
 
@@ -44,7 +47,7 @@ def run_mx(tg, A, B, SFA, SFB, out_dtype="bf16", add=None, pair=False):
     dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
     D = torch.full((A.shape[0], B.shape[0]), float("nan"), dtype=dt, device="cuda")
     tg.gemm_mxfp8_blockscaled(dev_u8(A), dev_u8(B), dev_u8(SFA), dev_u8(SFB), D,
-                              epilogue_add=add, cta_pair=pair)
+                              epilogue_add=add, cta_pair=bool(pair), multicast=pair == "mc")
     assert tg.tg_device_status()[0] == tg.TG_OK
     return D
 
@@ -55,7 +58,7 @@ def quarter_bits(rng, shape):
 
 # ------------------------------------------------------------------ bf16, small
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 def test_tiny_workload_full(tg, oracle, pair):
     x = synth.make_inputs("tiny")
     D = run_bf16(tg, x["A"], x["B"], "f32", pair=pair)
@@ -63,7 +66,7 @@ def test_tiny_workload_full(tg, oracle, pair):
     assert_within(host_values(D), ref, mag, False, "tiny")
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 512), (384, 256, 1024), (128, 256, 64)])
 def test_quarter_integers_bit_exact(tg, oracle, pair, M, N, K):
     rng = np.random.default_rng(M + N + K)
@@ -73,7 +76,7 @@ def test_quarter_integers_bit_exact(tg, oracle, pair, M, N, K):
     assert np.array_equal(host_values(D), ref)
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 def test_one_hot_across_tile_edges(tg, pair):
     M, N, K = 512, 512, 192
     one = 0x3F80
@@ -99,7 +102,7 @@ def test_identity(tg):
     assert np.array_equal(got, synth.bf16_bits_to_f32(A).astype(np.float64))
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N,K", [(1, 8, 16), (33, 40, 40), (130, 264, 72), (300, 520, 1000),
                                    (129, 8, 8)])
@@ -180,7 +183,7 @@ def mx_quarter(rng, shape):
     return synth.f32_to_e4m3fn_bits((rng.integers(-4, 5, shape) / 4).astype(np.float32))
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 def test_mx_small_full(tg, oracle, pair):
     x = synth.make_inputs("mx8k", M=256, N=512, K=512, seed=40)
     D = run_mx(tg, x["A"], x["B"], x["SFA"], x["SFB"], "bf16", pair=pair)
@@ -190,7 +193,7 @@ def test_mx_small_full(tg, oracle, pair):
     assert_within(host_values(D), ref, mag, False, "mx small f32")
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 def test_mx_unit_scales_quarter_integers_bit_exact(tg, oracle, pair):
     rng = np.random.default_rng(41)
     M, N, K = 256, 256, 384
@@ -202,7 +205,7 @@ def test_mx_unit_scales_quarter_integers_bit_exact(tg, oracle, pair):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 def test_mx_scales_reach_every_row_and_block(tg, oracle, pair):
     # Distinct power-of-two scales per (row, K block) on exact data: the
     # product is exact, so any misplaced scale byte changes some output.
@@ -216,7 +219,7 @@ def test_mx_scales_reach_every_row_and_block(tg, oracle, pair):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 @pytest.mark.parametrize("M,N,K", [(1, 16, 32), (100, 72, 96), (300, 264, 160)])
 def test_mx_ragged(tg, oracle, pair, M, N, K):
     x = synth.make_inputs("mx8k", M=M, N=N, K=K, seed=M + N + K)
