@@ -323,8 +323,13 @@ def run_ours(args, rank, world, local):
 
 
 def measure_e2e(torch, tg, host, dev, stream, steps, flops_step):
-    """Same step through the public API with pinned host buffers: H2D of the
-    step's inputs, the three calls, D2H of the three results, every step."""
+    """Same step through the public API with pinned host buffers, every step:
+    H2D of the step's inputs, the three calls, D2H of the three results.
+
+    Steps are pipelined the way a caller would use the C ABI: copies in,
+    compute and copies out run on three streams with two device buffer sets,
+    so step i's compute overlaps step i+1's inputs and step i-1's results.
+    """
     if steps <= 0:
         return None
     pin = {}
@@ -334,42 +339,71 @@ def measure_e2e(torch, tg, host, dev, stream, steps, flops_step):
                    ("X", host["tr"]["X"])):
         t = torch.from_numpy(arr.view(np.int16) if arr.dtype == np.uint16 else arr)
         pin[k] = t.pin_memory()
-    out_h = {
-        "D": torch.empty((SIZE, SIZE), dtype=torch.float32).pin_memory(),
-        "mD": torch.empty((SIZE, SIZE), dtype=torch.int16).pin_memory(),
-        "XT": torch.empty((SIZE, SIZE), dtype=torch.int16).pin_memory(),
-    }
-    devb = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pin.items()}
-    D = torch.empty((SIZE, SIZE), dtype=torch.float32, device=dev)
-    mD = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=dev)
-    XT = torch.empty((SIZE, SIZE), dtype=torch.int16, device=dev)
+    nb = 2
+    out_h = [{"D": torch.empty((SIZE, SIZE), dtype=torch.float32).pin_memory(),
+              "mD": torch.empty((SIZE, SIZE), dtype=torch.int16).pin_memory(),
+              "XT": torch.empty((SIZE, SIZE), dtype=torch.int16).pin_memory()} for _ in range(nb)]
+    ins = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pin.items()}
+           for _ in range(nb)]
+    outs = [{"D": torch.empty((SIZE, SIZE), dtype=torch.float32, device=dev),
+             "mD": torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=dev),
+             "XT": torch.empty((SIZE, SIZE), dtype=torch.int16, device=dev)} for _ in range(nb)]
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = sum(v.numel() * v.element_size() for v in out_h.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_h[0].values())
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()                                      # noqa: E731
+    in_done = [ev() for _ in range(nb)]
+    comp_done = [ev() for _ in range(nb)]
+    out_done = [ev() for _ in range(nb)]
+    for b in range(nb):                 # all buffers start free
+        comp_done[b].record(s_comp)
+        out_done[b].record(s_out)
 
-    def one():
-        for k in pin:
-            devb[k].copy_(pin[k], non_blocking=True)
-        tg.gemm_bf16(devb["A"].view(torch.bfloat16), devb["B"].view(torch.bfloat16), D,
-                     cta_pair=True, stream=stream)
-        tg.gemm_mxfp8_blockscaled(devb["mA"], devb["mB"], devb["SFA"], devb["SFB"], mD,
-                                  cta_pair=True, stream=stream)
-        tg.tile_transpose_b16(devb["X"], XT, stream=stream)
-        out_h["D"].copy_(D, non_blocking=True)
-        out_h["mD"].copy_(mD.view(torch.int16), non_blocking=True)
-        out_h["XT"].copy_(XT, non_blocking=True)
+    def one(i):
+        b = i % nb
+        d, o, oh = ins[b], outs[b], out_h[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(comp_done[b])          # inputs b no longer read
+            for k in pin:
+                d[k].copy_(pin[k], non_blocking=True)
+            in_done[b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_done[b])
+            s_comp.wait_event(out_done[b])         # results b already copied out
+            tg.gemm_bf16(d["A"].view(torch.bfloat16), d["B"].view(torch.bfloat16), o["D"],
+                         cta_pair=True, stream=s_comp)
+            tg.gemm_mxfp8_blockscaled(d["mA"], d["mB"], d["SFA"], d["SFB"], o["mD"],
+                                      cta_pair=True, stream=s_comp)
+            tg.tile_transpose_b16(d["X"], o["XT"], stream=s_comp)
+            comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            oh["D"].copy_(o["D"], non_blocking=True)
+            oh["mD"].copy_(o["mD"].view(torch.int16), non_blocking=True)
+            oh["XT"].copy_(o["XT"], non_blocking=True)
+            out_done[b].record(s_out)
 
-    one()
+    for i in range(nb):
+        one(i)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        one()
-    t1.record(stream)
+    t0.record(s_in)
+    s_comp.wait_event(t0)
+    s_out.wait_event(t0)
+    for i in range(steps):
+        one(i)
+    s_in.wait_stream(s_comp)
+    s_in.wait_stream(s_out)
+    t1.record(s_in)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
+    code, site = tg.tg_device_status()
+    if code != tg.TG_OK:
+        raise SystemExit(f"device status {code} (site {site}) in the end-to-end loop")
     return {"value": flops_step / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "pipelining": "3 streams (H2D / compute / D2H), 2 device buffer sets"}
 
 
 # ---------------------------------------------------------------------------
@@ -551,7 +585,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--configs", action="store_true",
                     help="time every workload of the table (one JSON line each) and exit")

@@ -5,19 +5,23 @@
 // elements (section "Transpose and stores": register element (row, 2w+h)
 // comes from shared element (2w+h, row), owned by lane 4*row + w), and
 // stmatrix writes a register image back to the rows its address providers
-// name (lane 8*matrix + row supplies that row's address).
+// name (lane 8*matrix + row supplies that row's address).  Tiles move with
+// TMA ("cp.async.bulk.tensor": descriptor-defined boxes, loads completing on
+// an mbarrier, stores as bulk groups; out-of-range elements of a load read
+// zero and out-of-range elements of a store are not written).
 //
-// Each CTA moves one 64 x 64 tile:
-//   1. ld.global.v4 (16-byte rows of 8 elements) -> shared tile S, where the
-//      16-byte chunk c of row r is stored at chunk c ^ (r % 8) so that the 8
-//      rows an ldmatrix phase touches fall in 8 different bank groups;
-//   2. per warp, two ldmatrix.x4.trans of S blocks (8w, 8c) -> registers now
-//      hold the transposed 8x8 blocks -> stmatrix.x4 into the output tile T at
-//      block (8c, 8w), with the same chunk swizzle;
-//   3. ld.shared.v4 rows of T -> st.global.v4 into out.
-// Edge tiles fall back to 16-bit loads / stores for the partial chunks.
+// Persistent kernel, two CTAs per SM, each walking 64 x 64 tiles through a
+// 4-stage ring:
+//   1. one thread TMA-loads the input tile into stage s with 128-byte
+//      swizzle: 16-byte chunk c of row r lands at chunk c ^ (r % 8), so the
+//      8 rows an ldmatrix phase touches fall in 8 different bank groups;
+//   2. each warp runs ldmatrix.x4.trans on S blocks (8w, 8c) and stmatrix.x4
+//      into the output tile at block (8c, 8w), same swizzle;
+//   3. one thread TMA-stores the output tile (edge tiles: element-wise stores
+//      inside the array) and refills stage s.
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "tg_internal.h"
@@ -29,90 +33,115 @@ namespace {
 
 constexpr int kTile = 64;
 constexpr int kThreads = 256;
+constexpr int kStages = 4;
+constexpr int kTileBytes = kTile * kTile * 2;     // 8 KB
+constexpr int kSmemBytes = 2 * kStages * kTileBytes + 1024 + 64;
+constexpr uint32_t kSiteTransposeFull = 20;
 
 __device__ __forceinline__ uint32_t chunk_offset(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kThreads)
-    transpose_b16_kernel(const uint16_t* __restrict__ in, int64_t ld_in,
-                         uint16_t* __restrict__ out, int64_t ld_out, int rows, int cols,
-                         int tiles_c) {
-  __shared__ __align__(128) uint8_t S[kTile * kTile * 2];
-  __shared__ __align__(128) uint8_t T[kTile * kTile * 2];
-  const int tile = blockIdx.x;
-  const int i0 = (tile / tiles_c) * kTile;   // input rows
-  const int j0 = (tile % tiles_c) * kTile;   // input columns
-  const int tid = threadIdx.x;
-  const bool full = (i0 + kTile <= rows) && (j0 + kTile <= cols);
+__global__ void __launch_bounds__(kThreads, 2)
+    transpose_b16_kernel(const __grid_constant__ CUtensorMap tm_in,
+                         const __grid_constant__ CUtensorMap tm_out, uint16_t* __restrict__ out,
+                         int64_t ld_out, int rows, int cols, int tiles_r, int tiles_c,
+                         uint32_t* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* in_tiles = smem;                             // [kStages][8 KB]
+  uint8_t* out_tiles = smem + kStages * kTileBytes;     // [kStages][8 KB]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 2 * kStages * kTileBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kStages);
 
-  // 1. global -> S
-  uint4 v[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int c = tid + q * kThreads;
-    const int r = c >> 3, ch = c & 7;
-    const int i = i0 + r, j = j0 + ch * 8;
-    if (full) {
-      v[q] = ld_global_nc_v4(in + static_cast<int64_t>(i) * ld_in + j);
-    } else {
-      uint32_t w[4] = {0, 0, 0, 0};
-      if (i < rows) {
-        const uint16_t* src = in + static_cast<int64_t>(i) * ld_in;
-        if (j + 8 <= cols) {
-          const uint4 t = ld_global_nc_v4(src + j);
-          w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (j + e < cols) w[e >> 1] |= static_cast<uint32_t>(src[j + e]) << (16 * (e & 1));
-        }
-      }
-      v[q] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int c = tid + q * kThreads;
-    *reinterpret_cast<uint4*>(S + chunk_offset(c >> 3, c & 7)) = v[q];
+  const int tid = threadIdx.x;
+  const int num_tiles = tiles_r * tiles_c;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tm_in);
+    prefetch_tensormap(&tm_out);
   }
   __syncthreads();
+  const WaitGuard guard{status, abort_flag, timeout_ns};
+  const uint64_t pol = policy_evict_first();
 
-  // 2. S -> registers (ldmatrix.trans) -> T (stmatrix)
-  {
-    const int w = tid >> 5;             // S block row (8 input rows)
-    const int lane = tid & 31;
-    const int m = lane >> 3, rr = lane & 7;
-    const uint32_t sS = smem_addr(S), sT = smem_addr(T);
+  auto issue_load = [&](int i, int s) {
+    const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    const int ti = t / tiles_c, tj = t % tiles_c;
+    mbar_arrive_expect_tx(&full[s], kTileBytes);
+    tma_load_2d(smem_addr(in_tiles + s * kTileBytes), &tm_in, smem_addr(&full[s]), tj * kTile,
+                ti * kTile, pol);
+  };
+  // This CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int my_tiles =
+      num_tiles > static_cast<int>(blockIdx.x)
+          ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+          : 0;
+  if (tid == 0)
+    for (int i = 0; i < kStages && i < my_tiles; ++i) issue_load(i, i);
+
+  const int w = tid >> 5, lane = tid & 31;
+  const int m = lane >> 3, rr = lane & 7;
+  bool ok = true;
+  for (int i = 0; i < my_tiles; ++i) {
+    const int s = i % kStages;
+    const uint32_t parity = static_cast<uint32_t>(i / kStages) & 1u;
+    if (!mbar_try_wait(smem_addr(&full[s]), parity) &&
+        !mbar_wait(&full[s], parity, guard, kSiteTransposeFull)) {
+      ok = false;
+    }
+    // The store that last read out[s] (kStages tiles ago) must be done.
+    if (tid == 0) bulk_wait_group_read<kStages - 1>();
+    __syncthreads();
+    if (!ok || *abort_flag) break;
+    const uint32_t sS = smem_addr(in_tiles + s * kTileBytes);
+    const uint32_t sT = smem_addr(out_tiles + s * kTileBytes);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int ch = 4 * h + m;         // S block column = T block row
+      const int ch = 4 * h + m;      // S block column = T block row
       uint32_t r0, r1, r2, r3;
       ldmatrix_x4_trans(sS + chunk_offset(8 * w + rr, ch), r0, r1, r2, r3);
       stmatrix_x4(sT + chunk_offset(8 * ch + rr, w), r0, r1, r2, r3);
     }
-  }
-  __syncthreads();
-
-  // 3. T -> global
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int c = tid + q * kThreads;
-    const int t = c >> 3, ch = c & 7;
-    const int oj = j0 + t, oi = i0 + ch * 8;
-    const uint4 x = *reinterpret_cast<const uint4*>(T + chunk_offset(t, ch));
-    if (full) {
-      st_global_v4(out + static_cast<int64_t>(oj) * ld_out + oi, x.x, x.y, x.z, x.w);
-    } else if (oj < cols) {
-      uint16_t* dst = out + static_cast<int64_t>(oj) * ld_out;
-      if (oi + 8 <= rows) {
-        st_global_v4(dst + oi, x.x, x.y, x.z, x.w);
-      } else {
+    // Shared writes (stmatrix) and reads (ldmatrix) -> async proxy (TMA).
+    fence_proxy_async_smem();
+    __syncthreads();
+    const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    const int ti = t / tiles_c, tj = t % tiles_c;
+    const bool full_tile = (ti + 1) * kTile <= rows && (tj + 1) * kTile <= cols;
+    if (!full_tile) {
+      // Edge tile: element-wise stores inside [cols, rows] only, so nothing
+      // outside the caller's array (its row padding included) is written.
+      const uint8_t* T = out_tiles + s * kTileBytes;
+      for (int c = tid; c < kTile * 8; c += kThreads) {
+        const int r = c >> 3, chunk = c & 7;
+        const int oj = tj * kTile + r, oi = ti * kTile + chunk * 8;
+        if (oj >= cols) continue;
+        const uint4 x = *reinterpret_cast<const uint4*>(T + chunk_offset(r, chunk));
         const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+        uint16_t* dst = out + static_cast<int64_t>(oj) * ld_out;
 #pragma unroll
         for (int e = 0; e < 8; ++e)
           if (oi + e < rows) dst[oi + e] = static_cast<uint16_t>(w4[e >> 1] >> (16 * (e & 1)));
       }
+      __syncthreads();     // out[s] is free again, in[s] was read above
+    }
+    if (tid == 0) {
+      if (full_tile) {
+        tma_store_2d(&tm_out, sT, ti * kTile, tj * kTile);
+        bulk_commit_group();
+      }
+      if (i + kStages < my_tiles) issue_load(i + kStages, s);
+    }
+  }
+  if (tid == 0) {
+    bulk_wait_group0();
+    if (!ok) {
+      // Gave up: let loads already issued land before the CTA exits.
+      for (int s = 0; s < kStages; ++s) mbar_wait_drain(&full[s], 0, timeout_ns);
     }
   }
 }
@@ -121,14 +150,34 @@ __global__ void __launch_bounds__(kThreads)
 
 int launch_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out, int64_t rows,
                          int64_t cols, cudaStream_t stream, DeviceCtx* ctx) {
-  (void)ctx;
   const int64_t tiles_r = (rows + kTile - 1) / kTile;
   const int64_t tiles_c = (cols + kTile - 1) / kTile;
+  if (tiles_r * tiles_c > 0x7FFFFFFF) return TG_ERR_UNSUPPORTED;
+  CUtensorMap tm_in, tm_out;
+  int rc = make_tensor_map_2d(&tm_in, CU_TENSOR_MAP_DATA_TYPE_UINT16, in,
+                              static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                              static_cast<uint64_t>(ld_in) * 2, kTile, kTile,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != TG_OK) return rc;
+  rc = make_tensor_map_2d(&tm_out, CU_TENSOR_MAP_DATA_TYPE_UINT16, out,
+                          static_cast<uint64_t>(rows), static_cast<uint64_t>(cols),
+                          static_cast<uint64_t>(ld_out) * 2, kTile, kTile,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != TG_OK) return rc;
+  static bool attr_set[64] = {};
+  if (!attr_set[ctx->device]) {
+    cudaError_t e = cudaFuncSetAttribute(transpose_b16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    attr_set[ctx->device] = true;
+  }
   const int64_t tiles = tiles_r * tiles_c;
-  if (tiles > 0x7FFFFFFF) return TG_ERR_UNSUPPORTED;
-  transpose_b16_kernel<<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(in), ld_in, static_cast<uint16_t*>(out), ld_out,
-      static_cast<int>(rows), static_cast<int>(cols), static_cast<int>(tiles_c));
+  int64_t grid = 2 * static_cast<int64_t>(ctx->num_sms);
+  if (grid > tiles) grid = tiles;
+  transpose_b16_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+      tm_in, tm_out, static_cast<uint16_t*>(out), ld_out, static_cast<int>(rows),
+      static_cast<int>(cols), static_cast<int>(tiles_r), static_cast<int>(tiles_c), ctx->status,
+      wait_timeout_ns());
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TG_OK : cuda_fail(e);
 }
