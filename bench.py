@@ -419,24 +419,7 @@ def run_configs(args):
     tgbuild.build()
     dev = torch.device("cuda", 0)
     peaks, _ = measured_peaks()
-    for name, w in synth.WORKLOADS.items():
-        x = synth.make_inputs(w)
-        if w.kind == "transpose":
-            X = torch.from_numpy(x["X"].view(np.int16)).to(dev)
-            out = torch.empty((w.N, w.M), dtype=torch.int16, device=dev)
-            fn = lambda: tg.tile_transpose_b16(X, out)           # noqa: E731
-        elif w.kind == "mxfp8":
-            A, B, SFA, SFB = (torch.from_numpy(x[k]).to(dev) for k in ("A", "B", "SFA", "SFB"))
-            D = torch.empty((w.M, w.N), device=dev,
-                            dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
-            fn = lambda: tg.gemm_mxfp8_blockscaled(A, B, SFA, SFB, D, cta_pair=w.cta_pair)  # noqa
-        else:
-            A = torch.from_numpy(x["A"].view(np.int16)).to(dev).view(torch.bfloat16)
-            B = torch.from_numpy(x["B"].view(np.int16)).to(dev).view(torch.bfloat16)
-            D = torch.empty((w.M, w.N), device=dev,
-                            dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
-            add = w.epi_add if w.epi_add else None
-            fn = lambda: tg.gemm_bf16(A, B, D, epilogue_add=add, cta_pair=w.cta_pair)  # noqa
+    def median_ms(fn):
         for _ in range(5):
             fn()
         torch.cuda.synchronize()
@@ -449,9 +432,40 @@ def run_configs(args):
             e1.record()
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    # Fused-epilogue rows: the same 8192^3 products with each non-trivial op.
+    bias = torch.linspace(-2.0, 2.0, SIZE, device=dev, dtype=torch.float32)
+    epilogue_rows = {"silu_affine": dict(silu_affine=(1.5, -0.25)), "bias": dict(bias=bias),
+                     "bias_silu": dict(bias=bias, bias_silu=True)}
+    rows = [(name, w, {}) for name, w in synth.WORKLOADS.items()]
+    rows += [(f"{base}+{op}", synth.WORKLOADS[base], kw) for base in ("sq8k", "mx8k")
+             for op, kw in epilogue_rows.items()]
+    for name, w, epi in rows:
+        x = synth.make_inputs(w)
+        if w.kind == "transpose":
+            X = torch.from_numpy(x["X"].view(np.int16)).to(dev)
+            out = torch.empty((w.N, w.M), dtype=torch.int16, device=dev)
+            fn = lambda: tg.tile_transpose_b16(X, out)           # noqa: E731
+        elif w.kind == "mxfp8":
+            A, B, SFA, SFB = (torch.from_numpy(x[k]).to(dev) for k in ("A", "B", "SFA", "SFB"))
+            D = torch.empty((w.M, w.N), device=dev,
+                            dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
+            fn = lambda: tg.gemm_mxfp8_blockscaled(A, B, SFA, SFB, D, cta_pair=w.cta_pair,  # noqa
+                                                   **epi)
+        else:
+            A = torch.from_numpy(x["A"].view(np.int16)).to(dev).view(torch.bfloat16)
+            B = torch.from_numpy(x["B"].view(np.int16)).to(dev).view(torch.bfloat16)
+            D = torch.empty((w.M, w.N), device=dev,
+                            dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
+            if not epi and w.epi_add:
+                epi = dict(epilogue_add=w.epi_add)
+            fn = lambda: tg.gemm_bf16(A, B, D, cta_pair=w.cta_pair, **epi)  # noqa: E731
+        ms = median_ms(fn)
         code, _ = tg.tg_device_status()
-        ms = statistics.median(times)
         line = {"workload": name, "describe": w.describe, "status": code, "ms_median": ms}
+        if epi:
+            line["epilogue"] = sorted(epi)
         if w.kind == "transpose":
             gbs = 2 * 2 * w.M * w.N / (ms * 1e-3) / 1e9
             line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]))
@@ -460,6 +474,8 @@ def run_configs(args):
             pk = float(peaks["bf16_tflops"]) * (2 if w.kind == "mxfp8" else 1)
             line.update(tflops=tf, frac_of_cublas_bf16_burst_scaled=tf / pk)
         print(json.dumps(line), flush=True)
+        del fn
+        torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------------------

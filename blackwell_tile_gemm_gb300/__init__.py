@@ -33,11 +33,20 @@ TG_D_F32 = 0
 TG_D_BF16 = 1
 TG_EPI_NONE = 0
 TG_EPI_ADD_SCALAR = 1
+TG_EPI_SILU_AFFINE = 2
+TG_EPI_BIAS_COL = 3
+TG_EPI_BIAS_COL_SILU = 4
 TG_FLAG_CTA_PAIR = 1
 TG_FLAG_MULTICAST = 2
 
 _lock = threading.Lock()
 _lib = None
+
+
+class tg_epilogue(ctypes.Structure):
+    """The C ABI's epilogue description (include/tgemm.h)."""
+    _fields_ = [("op", ctypes.c_int), ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("bias", ctypes.c_void_p)]
 
 
 class TgError(RuntimeError):
@@ -68,6 +77,13 @@ def lib() -> ctypes.CDLL:
         L.gemm_mxfp8_blockscaled.restype = i32
         L.gemm_mxfp8_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                              i64, i64, i64, i32, i32, ctypes.c_float, u32, vp]
+        L.gemm_bf16_ex.restype = i32
+        L.gemm_bf16_ex.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
+                                   ctypes.POINTER(tg_epilogue), u32, vp]
+        L.gemm_mxfp8_blockscaled_ex.restype = i32
+        L.gemm_mxfp8_blockscaled_ex.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                                i64, i64, i64, i32, ctypes.POINTER(tg_epilogue),
+                                                u32, vp]
         L.gemm_mxfp8_blockscaled_noalloc.restype = i32
         L.gemm_mxfp8_blockscaled_noalloc.argtypes = list(L.gemm_mxfp8_blockscaled.argtypes)
         L.tile_transpose_b16.restype = i32
@@ -135,14 +151,39 @@ def _flags(cta_pair, multicast):
     return (TG_FLAG_CTA_PAIR if cta_pair else 0) | (TG_FLAG_MULTICAST if multicast else 0)
 
 
-def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, cta_pair=False,
-              multicast=False, stream=None):
+def make_epilogue(epilogue_add=None, silu_affine=None, bias=None, bias_silu=False):
+    """Build the C epilogue description from keyword choices (at most one op).
+
+    epilogue_add=s: D = acc + s;  silu_affine=(scale, shift): D = silu(acc) *
+    scale + shift;  bias=<f32 CUDA tensor [N]>: D = acc + bias[j], or with
+    bias_silu=True D = silu(acc + bias[j]).
+    """
+    chosen = [epilogue_add is not None, silu_affine is not None, bias is not None]
+    if sum(chosen) > 1:
+        raise ValueError("choose one epilogue")
+    if epilogue_add is not None:
+        return tg_epilogue(TG_EPI_ADD_SCALAR, float(epilogue_add), 0.0, None)
+    if silu_affine is not None:
+        scale, shift = silu_affine
+        return tg_epilogue(TG_EPI_SILU_AFFINE, float(scale), float(shift), None)
+    if bias is not None:
+        import torch
+        if bias.dtype != torch.float32 or bias.dim() != 1 or not bias.is_contiguous():
+            raise TypeError("bias must be a contiguous float32 vector")
+        return tg_epilogue(TG_EPI_BIAS_COL_SILU if bias_silu else TG_EPI_BIAS_COL, 0.0, 0.0,
+                           bias.data_ptr())
+    return tg_epilogue(TG_EPI_NONE, 0.0, 0.0, None)
+
+
+def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, silu_affine=None, bias=None,
+              bias_silu=False, cta_pair=False, multicast=False, stream=None):
     """D[M,N] = A[M,K] @ B[N,K].T (+ epilogue_add), bf16 inputs, f32 accumulation.
 
     A, B: CUDA bfloat16 tensors with unit inner stride.  D: optional output
     (float32 or bfloat16, [M, N]); otherwise allocated with ``out_dtype``
     (default float32).  ``cta_pair`` selects the two-CTA (cta_group::2) kernel;
     ``multicast`` (with ``cta_pair``) runs clusters of two pairs sharing B.
+    Epilogue keywords: see ``make_epilogue``.
     """
     import torch
     M, K = A.shape
@@ -155,17 +196,19 @@ def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, cta_pair=False
         D = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
     if tuple(D.shape) != (M, N):
         raise ValueError("D must be [M, N]")
-    epi = TG_EPI_NONE if epilogue_add is None else TG_EPI_ADD_SCALAR
-    rc = lib().gemm_bf16(A.data_ptr(), _ld(A, "A", 8), B.data_ptr(), _ld(B, "B", 8),
-                         D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
-                         float(epilogue_add or 0.0), _flags(cta_pair, multicast),
-                         _stream_handle(stream))
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias must have N elements")
+    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu)
+    rc = lib().gemm_bf16_ex(A.data_ptr(), _ld(A, "A", 8), B.data_ptr(), _ld(B, "B", 8),
+                            D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype),
+                            ctypes.byref(epi), _flags(cta_pair, multicast), _stream_handle(stream))
     _check(rc, "gemm_bf16")
     return D
 
 
 def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_add=None,
-                           cta_pair=False, multicast=False, stream=None):
+                           silu_affine=None, bias=None, bias_silu=False, cta_pair=False,
+                           multicast=False, stream=None):
     """Block-scaled MXFP8 product: D = (A * 2^(SFA-127)) @ (B * 2^(SFB-127)).T.
 
     A: [M, K], B: [N, K] E4M3FN bytes (torch.float8_e4m3fn or uint8); SFA:
@@ -186,12 +229,14 @@ def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_a
         D = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=A.device)
     if tuple(D.shape) != (M, N):
         raise ValueError("D must be [M, N]")
-    epi = TG_EPI_NONE if epilogue_add is None else TG_EPI_ADD_SCALAR
-    rc = lib().gemm_mxfp8_blockscaled(
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias must have N elements")
+    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu)
+    rc = lib().gemm_mxfp8_blockscaled_ex(
         A.data_ptr(), _ld(A, "A", 16), B.data_ptr(), _ld(B, "B", 16),
         SFA.data_ptr(), _ld(SFA, "SFA", 1), SFB.data_ptr(), _ld(SFB, "SFB", 1),
-        D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), epi,
-        float(epilogue_add or 0.0), _flags(cta_pair, multicast), _stream_handle(stream))
+        D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), ctypes.byref(epi),
+        _flags(cta_pair, multicast), _stream_handle(stream))
     _check(rc, "gemm_mxfp8_blockscaled")
     return D
 

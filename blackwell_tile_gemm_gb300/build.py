@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtgemm.so")
 SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_mxfp8.cu", "gemm_mxfp8_noalloc.cu",
            "transpose.cu", "probes.cu"]
-HEADERS = ["tg_ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh", "tg_internal.h"]
+HEADERS = ["tg_ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh", "tg_internal.h", "epilogue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -143,22 +143,37 @@ void* device_workspace(size_t bytes) {
 
 int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
                 const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D,
-                int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
-                float epi_scalar, unsigned flags, cudaStream_t stream, DeviceCtx* ctx) {
-  const int epi_add = epilogue == TG_EPI_ADD_SCALAR ? 1 : 0;
-  if (K == 0)
-    return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi_add ? epi_scalar : 0.0f, stream);
+                int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, const Epi& epi,
+                unsigned flags, cudaStream_t stream, DeviceCtx* ctx) {
+  if (K == 0) return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi, stream);
   const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
   const bool mcast = (flags & TG_FLAG_MULTICAST) != 0;
   if (!mx)
     return launch_gemm_bf16_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M),
-                                 static_cast<int>(N), static_cast<int>(K), d_dtype, epi_add,
-                                 epi_scalar, pair, mcast, stream, ctx);
+                                 static_cast<int>(N), static_cast<int>(K), d_dtype, epi, pair,
+                                 mcast, stream, ctx);
   uint8_t* ws = static_cast<uint8_t*>(device_workspace(mxfp8_workspace_bytes(M, N, K, pair)));
   if (ws == nullptr) return TG_ERR_CUDA;
   return launch_gemm_mxfp8_impl(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
                                 static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                d_dtype, epi_add, epi_scalar, pair, mcast, ws, stream, ctx);
+                                d_dtype, epi, pair, mcast, ws, stream, ctx);
+}
+
+int check_epilogue(const tg_epilogue* epi, Epi* out) {
+  Epi e{kEpiNone, 0.0f, 0.0f, nullptr};
+  if (epi != nullptr) {
+    if (epi->op < kEpiNone || epi->op > kEpiBiasColSilu) return TG_ERR_INVALID_ARG;
+    e.op = epi->op;
+    e.alpha = epi->alpha;
+    e.beta = epi->beta;
+    if (epi_uses_bias(e.op)) {
+      if (epi->bias == nullptr) return TG_ERR_INVALID_ARG;
+      if (!aligned16(epi->bias)) return TG_ERR_MISALIGNED;
+      e.bias = epi->bias;
+    }
+  }
+  *out = e;
+  return TG_OK;
 }
 
 }  // namespace tg
@@ -175,7 +190,7 @@ int check_gemm_common(const void* A, int64_t lda, const void* B, int64_t ldb, vo
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return TG_ERR_INVALID_ARG;
   if (d_dtype != TG_D_F32 && d_dtype != TG_D_BF16) return TG_ERR_INVALID_ARG;
-  if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_ADD_SCALAR) return TG_ERR_INVALID_ARG;
+  if (epilogue < TG_EPI_NONE || epilogue > TG_EPI_BIAS_COL_SILU) return TG_ERR_INVALID_ARG;
   if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST))
     return TG_ERR_UNSUPPORTED;
   if ((flags & TG_FLAG_MULTICAST) && !(flags & TG_FLAG_CTA_PAIR)) return TG_ERR_INVALID_ARG;
@@ -214,32 +229,53 @@ int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb, con
 
 extern "C" {
 
-int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
-              int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue, float epi_scalar,
-              unsigned flags, void* cuda_stream) {
-  int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 2);
+int gemm_bf16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+                 int64_t M, int64_t N, int64_t K, int d_dtype, const tg_epilogue* epi,
+                 unsigned flags, void* cuda_stream) {
+  Epi e;
+  int rc = check_epilogue(epi, &e);
+  if (rc != TG_OK) return rc;
+  rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, TG_EPI_NONE, flags, 2);
   if (rc != TG_OK || M == 0 || N == 0) return rc;
   DeviceCtx* ctx = current_ctx();
   if (!ctx) return TG_ERR_CUDA;
-  return launch_gemm(false, A, lda, B, ldb, nullptr, 0, nullptr, 0, D, ldd, M, N, K, d_dtype,
-                     epilogue, epi_scalar, flags, as_stream(cuda_stream), ctx);
+  return launch_gemm(false, A, lda, B, ldb, nullptr, 0, nullptr, 0, D, ldd, M, N, K, d_dtype, e,
+                     flags, as_stream(cuda_stream), ctx);
+}
+
+int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+              int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue, float epi_scalar,
+              unsigned flags, void* cuda_stream) {
+  if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_ADD_SCALAR) return TG_ERR_INVALID_ARG;
+  const tg_epilogue e{epilogue, epi_scalar, 0.0f, nullptr};
+  return gemm_bf16_ex(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, &e, flags, cuda_stream);
+}
+
+int gemm_mxfp8_blockscaled_ex(const void* A, int64_t lda, const void* B, int64_t ldb,
+                              const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                              void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                              int d_dtype, const tg_epilogue* epi, unsigned flags,
+                              void* cuda_stream) {
+  Epi e;
+  int rc = check_epilogue(epi, &e);
+  if (rc != TG_OK) return rc;
+  rc = check_mxfp8_args(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K, d_dtype,
+                        TG_EPI_NONE, flags);
+  if (rc != TG_OK || M == 0 || N == 0) return rc;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  return launch_gemm(true, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K, d_dtype, e,
+                     flags, as_stream(cuda_stream), ctx);
 }
 
 int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
                            int epilogue, float epi_scalar, unsigned flags, void* cuda_stream) {
-  if (K % 32 != 0) return TG_ERR_INVALID_ARG;
-  int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 1);
-  if (rc != TG_OK || M == 0 || N == 0) return rc;
-  if (K > 0) {
-    if (SFA == nullptr || SFB == nullptr || ld_sfa < K / 32 || ld_sfb < K / 32)
-      return TG_ERR_INVALID_ARG;
-  }
-  DeviceCtx* ctx = current_ctx();
-  if (!ctx) return TG_ERR_CUDA;
-  return launch_gemm(true, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K, d_dtype,
-                     epilogue, epi_scalar, flags, as_stream(cuda_stream), ctx);
+  if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_ADD_SCALAR) return TG_ERR_INVALID_ARG;
+  const tg_epilogue e{epilogue, epi_scalar, 0.0f, nullptr};
+  return gemm_mxfp8_blockscaled_ex(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K,
+                                   d_dtype, &e, flags, cuda_stream);
 }
 
 int tile_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out, int64_t rows,

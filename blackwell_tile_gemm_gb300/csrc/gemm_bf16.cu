@@ -25,9 +25,8 @@ using CfgPairMcBf16 = GemmCfg<2, false, 256, 2, 6, true, true>;
 }  // namespace
 
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
-                          int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                          float epi_scalar, bool pair, bool mcast, cudaStream_t stream,
-                          DeviceCtx* ctx) {
+                          int64_t ldd, int M, int N, int K, int d_dtype, const Epi& epi,
+                          bool pair, bool mcast, cudaStream_t stream, DeviceCtx* ctx) {
   constexpr int BN = 256;
   const int g = pair ? 2 : 1;
   const int b_rows = BN / g;
@@ -48,8 +47,7 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
   a.num_k_blocks = ceil_div_i(K, 64);
   a.D = D;
   a.ldd = ldd;
-  a.epi_scalar = epi_scalar;
-  a.epi_add = epi_add;
+  a.epi = epi;
   a.raster_group = kRasterGroup;
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
@@ -69,28 +67,33 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
 // ---------------------------------------------------------------------------
 
 namespace {
-__global__ void fill_kernel(void* D, int64_t ldd, int64_t M, int64_t N, int bf16_out,
-                            float value) {
+__global__ void fill_kernel(void* D, int64_t ldd, int64_t M, int64_t N, int bf16_out, Epi epi) {
   const int64_t total = M * N;
-  const uint16_t vb = static_cast<uint16_t>(pack_bf16x2(value, value) & 0xFFFFu);
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / N, c = i % N;
+    float y = 0.0f;
+    if (epi.op == kEpiAddScalar)
+      y = epi.alpha;
+    else if (epi.op != kEpiNone)
+      y = apply_epi_general(epi.op, epi.alpha, epi.beta, 0.0f,
+                            epi_uses_bias(epi.op) ? epi.bias[c] : 0.0f);
     if (bf16_out)
-      reinterpret_cast<uint16_t*>(D)[r * ldd + c] = vb;
+      reinterpret_cast<uint16_t*>(D)[r * ldd + c] =
+          static_cast<uint16_t>(pack_bf16x2(y, y) & 0xFFFFu);
     else
-      reinterpret_cast<float*>(D)[r * ldd + c] = value;
+      reinterpret_cast<float*>(D)[r * ldd + c] = y;
   }
 }
 }  // namespace
 
-int launch_fill_epilogue(void* D, int64_t ldd, int64_t M, int64_t N, int d_dtype, float value,
+int launch_fill_epilogue(void* D, int64_t ldd, int64_t M, int64_t N, int d_dtype, const Epi& epi,
                          cudaStream_t stream) {
   const int64_t total = M * N;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(D, ldd, M, N,
-                                                                 d_dtype == TG_D_BF16, value);
+                                                                 d_dtype == TG_D_BF16, epi);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TG_OK : cuda_fail(e);
 }

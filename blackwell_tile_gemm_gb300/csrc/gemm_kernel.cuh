@@ -30,6 +30,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "epilogue.cuh"
 #include "tg_ptx.cuh"
 
 namespace tg {
@@ -49,8 +50,7 @@ struct GemmArgs {
   int num_k_blocks; // stages of BK elements
   void* D;
   int64_t ldd;
-  float epi_scalar;
-  int epi_add;      // 0: D = acc; 1: D = acc + epi_scalar
+  Epi epi;          // fused elementwise epilogue
   int sfa_blocks;   // 128-row blocks per K group in the SFA image
   int sfb_blocks;   // 128-row blocks per K group in the SFB image
   int raster_group; // m-tiles per band of the tile order
@@ -138,16 +138,58 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   tn = r / gm;
 }
 
-template <class C>
+// Four column biases starting at `c` (zeros past N).
+__device__ __forceinline__ float4 bias4(const GemmArgs& p, int c) {
+  if (c + 4 <= p.N) {
+    const uint4 q = ld_global_nc_v4(p.epi.bias + c);   // same address in every lane
+    return make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
+                       __uint_as_float(q.w));
+  }
+  float t[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) t[e] = c + e < p.N ? p.epi.bias[c + e] : 0.0f;
+  return make_float4(t[0], t[1], t[2], t[3]);
+}
+
+// SILU_AFFINE / BIAS_COL / BIAS_COL_SILU on 32 accumulator columns
+// [col0, col0+32) of one row, in place.  The op is uniform over the launch,
+// so each branch below runs without divergence.
+__device__ __forceinline__ void epilogue_general_chunk(const GemmArgs& p, int col0,
+                                                       uint32_t (&v)[32]) {
+  const int op = p.epi.op;
+  const float alpha = p.epi.alpha, beta = p.epi.beta;
+  if (op == kEpiSiluAffine) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      v[i] = __float_as_uint(apply_epi_general(kEpiSiluAffine, alpha, beta,
+                                               __uint_as_float(v[i]), 0.0f));
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 b = bias4(p, col0 + 4 * q);
+    const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      v[4 * q + e] = __float_as_uint(
+          apply_epi_general(op, alpha, beta, __uint_as_float(v[4 * q + e]), bb[e]));
+  }
+}
+
+// Stores 32 columns [col0, col0+32) of one row as D = v (+ add when kAdd),
+// 4 (f32) or 8 (bf16) columns per 16-byte store.
+template <class C, bool kAdd>
 __device__ __forceinline__ void epilogue_store_chunk(const GemmArgs& p, int row, int col0,
-                                                     const uint32_t (&v)[32], uint64_t pol) {
-  const float add = p.epi_add ? p.epi_scalar : 0.0f;
+                                                     const uint32_t (&v)[32], float add,
+                                                     uint64_t pol) {
   if constexpr (C::kBf16Out) {
     uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + static_cast<int64_t>(row) * p.ldd;
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) + add, __uint_as_float(v[2 * i + 1]) + add);
+      w[i] = kAdd ? pack_bf16x2(__uint_as_float(v[2 * i]) + add,
+                                __uint_as_float(v[2 * i + 1]) + add)
+                  : pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
     if (col0 + 32 <= p.N) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -171,7 +213,7 @@ __device__ __forceinline__ void epilogue_store_chunk(const GemmArgs& p, int row,
     float* drow = reinterpret_cast<float*>(p.D) + static_cast<int64_t>(row) * p.ldd;
     uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(v[i]) + add);
+    for (int i = 0; i < 32; ++i) w[i] = kAdd ? __float_as_uint(__uint_as_float(v[i]) + add) : v[i];
     if (col0 + 32 <= p.N) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -502,6 +544,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int half = (warp - 2) >> 2;                 // which BN/2 columns
     const int row_in_tile = slab * 32 + static_cast<int>(lane);
     const uint64_t pol_d = policy_evict_first();      // D is written once: keep A/B in L2
+    // NONE and ADD_SCALAR are folded into the stores; the other ops first
+    // transform the registers in place.
+    const bool epi_lean = p.epi.op == kEpiNone || p.epi.op == kEpiAddScalar;
+    const float epi_add = p.epi.op == kEpiAddScalar ? p.epi.alpha : 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t acce_remote = 0;
@@ -533,10 +579,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           mbar_arrive_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
       }
       const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
+      const int col_base = tn * C::BN + half * C::kEpiCols;
+      if (epi_lean) {
 #pragma unroll
-      for (int c = 0; c < C::kEpiChunks; ++c) {
-        const int col0 = tn * C::BN + half * C::kEpiCols + 32 * c;
-        if (row < p.M && col0 < p.N) epilogue_store_chunk<C>(p, row, col0, v[c], pol_d);
+        for (int c = 0; c < C::kEpiChunks; ++c) {
+          const int col0 = col_base + 32 * c;
+          if (row < p.M && col0 < p.N)
+            epilogue_store_chunk<C, true>(p, row, col0, v[c], epi_add, pol_d);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::kEpiChunks; ++c) {
+          const int col0 = col_base + 32 * c;
+          if (row < p.M && col0 < p.N) {
+            epilogue_general_chunk(p, col0, v[c]);
+            epilogue_store_chunk<C, false>(p, row, col0, v[c], 0.0f, pol_d);
+          }
+        }
       }
       if (++acc == C::kAccBufs) {
         acc = 0;

@@ -106,8 +106,8 @@ size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair) {
 
 int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
-                           void* D, int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                           float epi_scalar, bool pair, bool mcast, uint8_t* sf_workspace,
+                           void* D, int64_t ldd, int M, int N, int K, int d_dtype,
+                           const Epi& epi, bool pair, bool mcast, uint8_t* sf_workspace,
                            cudaStream_t stream, DeviceCtx* ctx) {
   const MxPlan pl = plan_mx(M, N, K, pair);
   const int g = pair ? 2 : 1;
@@ -151,8 +151,7 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
   a.num_k_blocks = pl.num_kg;
   a.D = D;
   a.ldd = ldd;
-  a.epi_scalar = epi_scalar;
-  a.epi_add = epi_add;
+  a.epi = epi;
   a.sfa_blocks = pl.sfa_blocks;
   a.sfb_blocks = pl.sfb_blocks;
   a.raster_group = kRasterGroup;

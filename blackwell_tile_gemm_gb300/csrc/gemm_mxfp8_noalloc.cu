@@ -83,13 +83,13 @@ extern "C" int gemm_mxfp8_blockscaled_noalloc(const void* A, int64_t lda, const 
                                               int64_t ldd, int64_t M, int64_t N, int64_t K,
                                               int d_dtype, int epilogue, float epi_scalar,
                                               unsigned flags, void* cuda_stream) {
+  if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_ADD_SCALAR) return TG_ERR_INVALID_ARG;
   int rc = check_mxfp8_args(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K, d_dtype,
                             epilogue, flags);
   if (rc != TG_OK || M == 0 || N == 0) return rc;
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  const int epi_add = epilogue == TG_EPI_ADD_SCALAR ? 1 : 0;
-  if (K == 0)
-    return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi_add ? epi_scalar : 0.0f, stream);
+  const Epi epi{epilogue, epi_scalar, 0.0f, nullptr};
+  if (K == 0) return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi, stream);
   const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
   if (mxfp8_workspace_bytes(M, N, K, pair) > kNoAllocScratchBytes) return TG_ERR_NO_SCRATCH;
   DeviceCtx* ctx = current_ctx();
@@ -98,6 +98,6 @@ extern "C" int gemm_mxfp8_blockscaled_noalloc(const void* A, int64_t lda, const 
   if (scratch == nullptr) return rc;
   return launch_gemm_mxfp8_impl(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
                                 static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                d_dtype, epi_add, epi_scalar, pair,
-                                (flags & TG_FLAG_MULTICAST) != 0, scratch, stream, ctx);
+                                d_dtype, epi, pair, (flags & TG_FLAG_MULTICAST) != 0, scratch,
+                                stream, ctx);
 }

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/tgemm.h"
+#include "epilogue.cuh"
 
 namespace tg {
 
@@ -40,18 +41,20 @@ void* device_workspace(size_t bytes);
 // Launchers (arguments already validated).
 int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
                 const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D,
-                int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
-                float epi_scalar, unsigned flags, cudaStream_t stream, DeviceCtx* ctx);
+                int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, const Epi& epi,
+                unsigned flags, cudaStream_t stream, DeviceCtx* ctx);
+
+// Host checks of an epilogue description (no CUDA calls); fills `out`.
+int check_epilogue(const tg_epilogue* epi, Epi* out);
 
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
-                          int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                          float epi_scalar, bool pair, bool mcast, cudaStream_t stream,
-                          DeviceCtx* ctx);
+                          int64_t ldd, int M, int N, int K, int d_dtype, const Epi& epi,
+                          bool pair, bool mcast, cudaStream_t stream, DeviceCtx* ctx);
 
 int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
-                           void* D, int64_t ldd, int M, int N, int K, int d_dtype, int epi_add,
-                           float epi_scalar, bool pair, bool mcast, uint8_t* sf_workspace,
+                           void* D, int64_t ldd, int M, int N, int K, int d_dtype,
+                           const Epi& epi, bool pair, bool mcast, uint8_t* sf_workspace,
                            cudaStream_t stream, DeviceCtx* ctx);
 
 // Host-side argument checks of the block-scaled call (no CUDA calls).
@@ -65,7 +68,7 @@ int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb, con
 size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair);
 
 // D = epilogue(0) when K == 0.
-int launch_fill_epilogue(void* D, int64_t ldd, int64_t M, int64_t N, int d_dtype, float value,
+int launch_fill_epilogue(void* D, int64_t ldd, int64_t M, int64_t N, int d_dtype, const Epi& epi,
                          cudaStream_t stream);
 
 int launch_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out, int64_t rows,

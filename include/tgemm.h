@@ -58,9 +58,31 @@ typedef enum {
 /* Element type of D. */
 enum { TG_D_F32 = 0, TG_D_BF16 = 1 };
 
-/* Fused elementwise epilogue, applied to the f32 accumulator before the
- * conversion to D's type [EW]:  NONE: D = acc;  ADD_SCALAR: D = acc + s. */
-enum { TG_EPI_NONE = 0, TG_EPI_ADD_SCALAR = 1 };
+/* Fused elementwise epilogue, applied per element to the f32 accumulator
+ * `acc` of output (i, j) before the conversion to D's type [EW]:
+ *   TG_EPI_NONE           D = acc
+ *   TG_EPI_ADD_SCALAR     D = acc + alpha
+ *   TG_EPI_SILU_AFFINE    D = silu(acc) * alpha + beta      (the pages' silu_affine)
+ *   TG_EPI_BIAS_COL       D = acc + bias[j]
+ *   TG_EPI_BIAS_COL_SILU  D = silu(acc + bias[j])
+ * with silu(x) = x / (1 + exp(-x)) evaluated in f32 (CUDA expf). */
+enum {
+  TG_EPI_NONE = 0,
+  TG_EPI_ADD_SCALAR = 1,
+  TG_EPI_SILU_AFFINE = 2,
+  TG_EPI_BIAS_COL = 3,
+  TG_EPI_BIAS_COL_SILU = 4
+};
+
+/* Epilogue description for the *_ex entry points (caller-owned, read during
+ * the call only).  bias: device f32 [N], 16-byte aligned, used by the
+ * BIAS_COL ops only (NULL otherwise); alpha/beta as in the table above. */
+typedef struct tg_epilogue {
+  int op;
+  float alpha;
+  float beta;
+  const float* bias;
+} tg_epilogue;
 
 /* Launch flags (bit set). */
 enum {
@@ -82,7 +104,8 @@ enum {
  *   M,N,K: sizes, 0 <= M, N, K < 2^31.  M or N == 0: nothing is launched.
  *          K == 0: D = epilogue(0).  Any size need not be a tile multiple:
  *          loads past the edge read zeros [TMA], stores past it are dropped.
- *   epilogue, epi_scalar: TG_EPI_NONE or TG_EPI_ADD_SCALAR with constant s.
+ *   epilogue, epi_scalar: TG_EPI_NONE, or TG_EPI_ADD_SCALAR with constant s
+ *          (the other epilogues need gemm_bf16_ex).
  *   flags: 0, TG_FLAG_CTA_PAIR, or TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST
  *          (TG_FLAG_MULTICAST alone: TG_ERR_INVALID_ARG).
  * Rounding: f32 -> bf16 D is round-to-nearest-even.  Alignment: A, B, D
@@ -92,6 +115,17 @@ enum {
 int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
               int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue, float epi_scalar,
               unsigned flags, void* cuda_stream);
+
+/*
+ * gemm_bf16_ex -- gemm_bf16 with a full epilogue description.  epi may be
+ * NULL (D = acc).  An unknown op, or a BIAS_COL op without a bias vector,
+ * returns TG_ERR_INVALID_ARG; a bias not 16-byte aligned TG_ERR_MISALIGNED.
+ * gemm_bf16(..., epilogue, s, ...) equals gemm_bf16_ex with {epilogue, s, 0,
+ * NULL} and accepts only TG_EPI_NONE and TG_EPI_ADD_SCALAR.
+ */
+int gemm_bf16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+                 int64_t M, int64_t N, int64_t K, int d_dtype, const tg_epilogue* epi,
+                 unsigned flags, void* cuda_stream);
 
 /*
  * gemm_mxfp8_blockscaled -- block-scaled MXFP8 product [MMA, .block_scale]:
@@ -113,6 +147,14 @@ int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ld
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
                            int epilogue, float epi_scalar, unsigned flags, void* cuda_stream);
+
+/* gemm_mxfp8_blockscaled_ex -- gemm_mxfp8_blockscaled with a full epilogue
+ * description (as gemm_bf16_ex). */
+int gemm_mxfp8_blockscaled_ex(const void* A, int64_t lda, const void* B, int64_t ldb,
+                              const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                              void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                              int d_dtype, const tg_epilogue* epi, unsigned flags,
+                              void* cuda_stream);
 
 /*
  * gemm_mxfp8_blockscaled_noalloc -- the same product as gemm_mxfp8_blockscaled,

@@ -20,6 +20,9 @@ Contents, each following the page it cites (TVM TIRx documentation):
 * ``tmem_register_coord`` -- the tcgen05.ld/st register images ("Explicit
   CUDA tile patterns", section "TMEM transfers").
 * ``add_one`` -- the elementwise example ("Tile Operands and Execution").
+* ``apply_epilogue`` -- the fused elementwise epilogues (``silu_affine`` from
+  "Explicit CUDA tile patterns", section "Scalar compositions"; a constant; a
+  per-column bias), in float64 on the float64 contraction.
 """
 from __future__ import annotations
 
@@ -214,6 +217,41 @@ def transpose_b16(X: np.ndarray) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"tgo_transpose_b16 rejected its arguments (code {rc})")
     return out
+
+
+# Epilogue operation codes (the values of the library's C ABI, restated).
+EPI_NONE, EPI_ADD_SCALAR, EPI_SILU_AFFINE, EPI_BIAS_COL, EPI_BIAS_COL_SILU = 0, 1, 2, 3, 4
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """silu(x) = x / (1 + exp(-x)), in float64 (the pages' silu_affine body)."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def apply_epilogue(ref: np.ndarray, op: int, alpha: float = 0.0, beta: float = 0.0,
+                   bias=None, cols=None) -> np.ndarray:
+    """The fused epilogue on a float64 result block ``ref`` [rows, ncols].
+
+    NONE: ref; ADD_SCALAR: ref + alpha; SILU_AFFINE: silu(ref) * alpha + beta;
+    BIAS_COL: ref + bias[j]; BIAS_COL_SILU: silu(ref + bias[j]).  ``bias`` is
+    the full per-column vector (length N); ``cols`` lists which columns the
+    block holds (default: all, in order).
+    """
+    ref = np.asarray(ref, dtype=np.float64)
+    if op == EPI_NONE:
+        return ref.copy()
+    if op == EPI_ADD_SCALAR:
+        return ref + float(alpha)
+    if op == EPI_SILU_AFFINE:
+        return silu(ref) * float(alpha) + float(beta)
+    if op in (EPI_BIAS_COL, EPI_BIAS_COL_SILU):
+        b = np.asarray(bias, dtype=np.float64)
+        b = b if cols is None else b[np.asarray(cols)]
+        x = ref + b[None, :]
+        return x if op == EPI_BIAS_COL else silu(x)
+    raise ValueError(f"unknown epilogue op {op}")
 
 
 def add_one(a: np.ndarray) -> np.ndarray:

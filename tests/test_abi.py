@@ -100,3 +100,27 @@ def test_transpose_rejects_bad_arguments(L):
     assert f(A16 + 2, 64, A16 * 4, 64, 64, 64, None) == tg.TG_ERR_MISALIGNED
     assert f(A16, 32, A16 * 4, 64, 64, 64, None) == tg.TG_ERR_INVALID_ARG    # ld_in < cols
     assert f(A16, 64, A16 + 64, 64, 64, 64, None) == tg.TG_ERR_INVALID_ARG  # overlap
+
+
+@pytest.mark.parametrize("op,bias,code", [
+    (5, 0, tg.TG_ERR_INVALID_ARG),                  # unknown op
+    (-1, 0, tg.TG_ERR_INVALID_ARG),
+    (tg.TG_EPI_BIAS_COL, 0, tg.TG_ERR_INVALID_ARG),  # bias op without a bias
+    (tg.TG_EPI_BIAS_COL_SILU, A16 + 4, tg.TG_ERR_MISALIGNED),
+])
+def test_gemm_ex_rejects_bad_epilogues(L, op, bias, code):
+    epi = tg.tg_epilogue(op, 0.0, 0.0, bias or None)
+    for f, extra in ((L.gemm_bf16_ex, ()), (L.gemm_mxfp8_blockscaled_ex, (A16, 2, A16, 2))):
+        head = (A16, 64, A16, 64) + extra
+        assert f(*head, A16, 64, 64, 64, 64, 0, ctypes.byref(epi), 0, None) == code
+
+
+def test_gemm_ex_accepts_a_null_epilogue_for_empty_problems(L):
+    assert L.gemm_bf16_ex(0, 0, 0, 0, 0, 0, 0, 64, 64, 0, None, 0, None) == tg.TG_OK
+
+
+def test_make_epilogue_rejects_two_ops():
+    with pytest.raises(ValueError):
+        tg.make_epilogue(epilogue_add=1.0, silu_affine=(1.0, 0.0))
+    e = tg.make_epilogue(silu_affine=(2.0, -1.0))
+    assert (e.op, e.alpha, e.beta) == (tg.TG_EPI_SILU_AFFINE, 2.0, -1.0)

@@ -369,3 +369,39 @@ def test_add_one_worked_example(oracle):
     a = np.arange(768, dtype=np.float32).reshape(2, 32, 3, 4)
     golden = np.loadtxt(os.path.join(GOLDEN, "add_one_2x32x3x4.txt"), dtype=np.float32)
     assert np.array_equal(oracle.add_one(a).reshape(-1), golden.reshape(-1))
+
+
+# ---------------------------------------------------------------------------
+# fused epilogues
+# ---------------------------------------------------------------------------
+
+def test_silu_matches_library_logistic(oracle):
+    special = pytest.importorskip("scipy.special")
+    x = np.concatenate([np.linspace(-40, 40, 2001), [0.0, 1e-8, -1e-8, 700.0, -700.0]])
+    assert np.allclose(oracle.silu(x), x * special.expit(x), rtol=1e-14, atol=1e-300)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+
+
+def test_silu_reflection_identity(oracle):
+    # silu(-x) = -x * sigmoid(-x) = silu(x) - x
+    x = np.linspace(-30, 30, 601)
+    assert np.allclose(oracle.silu(-x), oracle.silu(x) - x, rtol=1e-12, atol=1e-12)
+
+
+def test_epilogue_ops_closed_forms(oracle):
+    rng = np.random.default_rng(20)
+    ref = rng.standard_normal((5, 7)) * 3
+    bias = rng.standard_normal(11)
+    cols = [0, 3, 4, 6, 8, 9, 10]
+    assert np.array_equal(oracle.apply_epilogue(ref, oracle.EPI_NONE), ref)
+    assert np.array_equal(oracle.apply_epilogue(ref, oracle.EPI_ADD_SCALAR, 1.0), ref + 1)
+    sa = oracle.apply_epilogue(ref, oracle.EPI_SILU_AFFINE, 2.0, 1.0)
+    assert np.allclose(sa, 2 * ref / (1 + np.exp(-ref)) + 1, rtol=1e-15)
+    bc = oracle.apply_epilogue(ref, oracle.EPI_BIAS_COL, bias=bias, cols=cols)
+    for jj, j in enumerate(cols):
+        assert np.array_equal(bc[:, jj], ref[:, jj] + bias[j])
+    bs = oracle.apply_epilogue(ref, oracle.EPI_BIAS_COL_SILU, bias=bias, cols=cols)
+    assert np.allclose(bs, oracle.silu(bc), rtol=0, atol=0)
+    # the add-one example is the ADD_SCALAR op with alpha = 1
+    a = np.arange(768, dtype=np.float64).reshape(64, 12)
+    assert np.array_equal(oracle.apply_epilogue(a, oracle.EPI_ADD_SCALAR, 1.0), a + 1)
