@@ -103,6 +103,50 @@ def e8m0_scales(rng: np.random.Generator, shape, lo=-4, hi=4) -> np.ndarray:
     return (127 + rng.integers(lo, hi + 1, size=shape)).astype(np.uint8)
 
 
+# E2M1 magnitudes by 3-bit code (exponent bias 1, one fraction bit).
+_E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def f32_to_e2m1_codes(x: np.ndarray) -> np.ndarray:
+    """Round to FP4 E2M1 (nearest, ties to the even code), saturating at +-6;
+    one 4-bit code per uint8 (sign in bit 3)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 6.0)
+    # nearest magnitude; on an exact midpoint take the code with fraction bit 0
+    d = np.abs(a[..., None] - _E2M1_MAGNITUDES)
+    best = np.argmin(d + (np.arange(8) & 1) * 1e-12, axis=-1).astype(np.uint8)
+    sign = (np.signbit(x) & (best != 0)).astype(np.uint8)
+    return (sign << 3) | best
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """[rows, K] 4-bit codes -> [rows, K/2] bytes, element 2i in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    if c.shape[-1] % 2:
+        raise ValueError("K must be even")
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
+    """Inverse of pack_e2m1."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def e2m1_normal_packed(rng: np.random.Generator, shape, sigma: float = 2.0) -> np.ndarray:
+    """Packed E2M1 of N(0, sigma^2) samples; shape is the unpacked [rows, K]."""
+    x = rng.standard_normal(size=shape, dtype=np.float32) * np.float32(sigma)
+    return pack_e2m1(f32_to_e2m1_codes(x))
+
+
+def ue4m3_pow2_scales(rng: np.random.Generator, shape, lo=-3, hi=3) -> np.ndarray:
+    """UE4M3 bytes of 2^U{lo..hi} (exact in E4M3: exponent field 7 + u, fraction 0)."""
+    return ((7 + rng.integers(lo, hi + 1, size=shape)) << 3).astype(np.uint8)
+
+
 def b16_bits(rng: np.random.Generator, shape) -> np.ndarray:
     return rng.integers(0, 1 << 16, size=shape, dtype=np.uint16)
 
@@ -114,7 +158,7 @@ def b16_bits(rng: np.random.Generator, shape) -> np.ndarray:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str          # "bf16", "mxfp8" or "transpose"
+    kind: str          # "bf16", "mxfp8", "mxfp4", "nvfp4" or "transpose"
     M: int
     N: int
     K: int
@@ -142,6 +186,10 @@ WORKLOADS = {
                        "bf16 GEMM 4000x3000x1000 + 1, U[-1,1) inputs, fp32 D"),
     "tr8k": Workload("tr8k", "transpose", 8192, 8192, 0, 6, "b16", 0.0, False,
                      "b16 transpose 8192x8192, random bit patterns"),
+    "mxf4_8k": Workload("mxf4_8k", "mxfp4", 8192, 8192, 8192, 7, "bf16", 0.0, True,
+                        "MXFP4 GEMM 8192^3, E2M1 x E8M0/32 inputs, bf16 D"),
+    "nvf4_8k": Workload("nvf4_8k", "nvfp4", 8192, 8192, 8192, 8, "bf16", 0.0, True,
+                        "NVFP4 GEMM 8192^3, E2M1 x UE4M3/16 inputs, bf16 D"),
 }
 
 
@@ -152,6 +200,9 @@ def make_inputs(w: Workload | str, M: int | None = None, N: int | None = None,
     bf16:      {"A": uint16 [M,K], "B": uint16 [N,K]}
     mxfp8:     {"A": uint8 [M,K], "B": uint8 [N,K], "SFA": uint8 [M,K/32],
                 "SFB": uint8 [N,K/32]}
+    mxfp4:     {"A": uint8 [M,K/2] packed E2M1, "B": uint8 [N,K/2],
+                "SFA": uint8 [M,K/32] E8M0, "SFB": uint8 [N,K/32]}
+    nvfp4:     as mxfp4 with "SFA": uint8 [M,K/16] UE4M3, "SFB": uint8 [N,K/16]
     transpose: {"X": uint16 [M,N]}
     """
     if isinstance(w, str):
@@ -168,6 +219,20 @@ def make_inputs(w: Workload | str, M: int | None = None, N: int | None = None,
             "B": e4m3_normal(rng, (N, K)),
             "SFA": e8m0_scales(rng, (M, K // 32)),
             "SFB": e8m0_scales(rng, (N, K // 32)),
+        }
+    if w.kind == "mxfp4":
+        return {
+            "A": e2m1_normal_packed(rng, (M, K)),
+            "B": e2m1_normal_packed(rng, (N, K)),
+            "SFA": e8m0_scales(rng, (M, K // 32), -3, 3),
+            "SFB": e8m0_scales(rng, (N, K // 32), -3, 3),
+        }
+    if w.kind == "nvfp4":
+        return {
+            "A": e2m1_normal_packed(rng, (M, K)),
+            "B": e2m1_normal_packed(rng, (N, K)),
+            "SFA": ue4m3_pow2_scales(rng, (M, K // 16)),
+            "SFB": ue4m3_pow2_scales(rng, (N, K // 16)),
         }
     if w.name in ("tiny", "ragged"):
         return {"A": bf16_uniform(rng, (M, K)), "B": bf16_uniform(rng, (N, K))}

@@ -7,9 +7,10 @@ them: the two sides share no code, only the seeded input generators.
 
 Contents, each following the page it cites (TVM TIRx documentation):
 
-* ``gemm_bf16`` / ``gemm_mxfp8`` -- float64 triple loop in ``tg_oracle.c``
-  ("tcgen05.mma", section "Examples": B stored as (N, K), result a @ b.T;
-  block scaling from section "Weight-stationary and block scaling").
+* ``gemm_bf16`` / ``gemm_mxfp8`` / ``gemm_mxfp4`` / ``gemm_nvfp4`` -- float64
+  triple loop in ``tg_oracle.c`` ("tcgen05.mma", section "Examples": B stored
+  as (N, K), result a @ b.T; block scaling from section "Weight-stationary
+  and block scaling", with .scale_vec::1X / 2X / 4X).
 * ``transpose_b16`` -- out[j, i] = in[i, j] on raw 16-bit patterns.
 * ``ldmatrix_image`` -- the register image of ``ldmatrix.m8n8.xN[.trans]``
   ("ldmatrix / stmatrix", sections "Address providers and result owners"
@@ -72,7 +73,12 @@ def _load():
         lib.tgo_e4m3fn_to_f64.argtypes = [ctypes.c_uint8]
         lib.tgo_e8m0_to_f64.restype = ctypes.c_double
         lib.tgo_e8m0_to_f64.argtypes = [ctypes.c_uint8]
-        for name in ("tgo_decode_bf16", "tgo_decode_e4m3fn", "tgo_decode_e8m0"):
+        lib.tgo_e2m1_to_f64.restype = ctypes.c_double
+        lib.tgo_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.tgo_ue4m3_to_f64.restype = ctypes.c_double
+        lib.tgo_ue4m3_to_f64.argtypes = [ctypes.c_uint8]
+        for name in ("tgo_decode_bf16", "tgo_decode_e4m3fn", "tgo_decode_e8m0",
+                     "tgo_decode_e2m1", "tgo_decode_ue4m3"):
             getattr(lib, name).restype = None
             getattr(lib, name).argtypes = [dp, i64, dp]
         lib.tgo_gemm_bf16.restype = ctypes.c_int
@@ -82,6 +88,10 @@ def _load():
         lib.tgo_gemm_mxfp8.argtypes = [dp, i64, dp, i64, dp, i64, dp, i64,
                                        i64, i64, i64, ctypes.c_double,
                                        dp, i64, dp, i64, dp, dp]
+        lib.tgo_gemm_fp4.restype = ctypes.c_int
+        lib.tgo_gemm_fp4.argtypes = [dp, i64, dp, i64, dp, i64, dp, i64,
+                                     i64, i64, i64, ctypes.c_int, ctypes.c_double,
+                                     dp, i64, dp, i64, dp, dp]
         lib.tgo_transpose_b16.restype = ctypes.c_int
         lib.tgo_transpose_b16.argtypes = [dp, i64, dp, i64, i64, i64]
         lib.tgo_num_threads.restype = ctypes.c_int
@@ -126,6 +136,21 @@ def decode_e8m0(bits: np.ndarray) -> np.ndarray:
     b = np.ascontiguousarray(bits, dtype=np.uint8)
     out = np.empty(b.shape, dtype=np.float64)
     _load().tgo_decode_e8m0(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def decode_e2m1(nibbles: np.ndarray) -> np.ndarray:
+    """E2M1 values of the low 4 bits of each byte."""
+    b = np.ascontiguousarray(nibbles, dtype=np.uint8)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().tgo_decode_e2m1(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def decode_ue4m3(bits: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().tgo_decode_ue4m3(_ptr(b), b.size, _ptr(out))
     return out
 
 
@@ -204,6 +229,55 @@ def gemm_mxfp8(A, B, SFA, SFB, add: float = 0.0, rows=None, cols=None):
     return ref, mag
 
 
+FP4_MX, FP4_NV = 0, 1     # scale kinds: E8M0 per 32 (MXFP4), UE4M3 per 16 (NVFP4)
+
+
+def gemm_fp4(A, B, SFA, SFB, scale_kind: int, add: float = 0.0, rows=None, cols=None):
+    """float64 oracle of the block-scaled FP4 product over raw bytes.
+
+    A: uint8 [M, K/2] packed E2M1 (element 2i in the low nibble of byte i);
+    B: uint8 [N, K/2].  scale_kind FP4_MX: SFA uint8 [M, K/32] E8M0;
+    FP4_NV: SFA uint8 [M, K/16] UE4M3 (SFB likewise).
+    a_ik = e2m1(A_ik) * scale(SFA[i, k // block]), likewise b; D = a @ b.T (+ add).
+    """
+    block = {FP4_MX: 32, FP4_NV: 16}[scale_kind]
+    arrs = []
+    for X in (A, B, SFA, SFB):
+        X = np.asarray(X)
+        if X.dtype != np.uint8 or X.ndim != 2:
+            raise TypeError("gemm_fp4 oracle takes 2-D uint8 arrays")
+        if X.strides[1] != 1:
+            X = np.ascontiguousarray(X)
+        arrs.append(X)
+    A, B, SFA, SFB = arrs
+    M, K = A.shape[0], 2 * A.shape[1]
+    N = B.shape[0]
+    if B.shape[1] != K // 2 or K % block or SFA.shape != (M, K // block) or \
+            SFB.shape != (N, K // block):
+        raise ValueError("shape mismatch for the block-scaled FP4 product")
+    r, nr = _index_list(rows, M)
+    c, nc = _index_list(cols, N)
+    ref = np.empty((nr, nc), dtype=np.float64)
+    mag = np.empty((nr, nc), dtype=np.float64)
+    rc = _load().tgo_gemm_fp4(_ptr(A), A.strides[0], _ptr(B), B.strides[0],
+                              _ptr(SFA), SFA.strides[0], _ptr(SFB), SFB.strides[0],
+                              M, N, K, int(scale_kind), float(add), _ptr(r), nr, _ptr(c), nc,
+                              _ptr(ref), _ptr(mag))
+    if rc != 0:
+        raise ValueError(f"tgo_gemm_fp4 rejected its arguments (code {rc})")
+    return ref, mag
+
+
+def gemm_mxfp4(A, B, SFA, SFB, add: float = 0.0, rows=None, cols=None):
+    """MXFP4: packed E2M1 operands, one E8M0 scale per 32 K elements."""
+    return gemm_fp4(A, B, SFA, SFB, FP4_MX, add, rows, cols)
+
+
+def gemm_nvfp4(A, B, SFA, SFB, add: float = 0.0, rows=None, cols=None):
+    """NVFP4: packed E2M1 operands, one UE4M3 scale per 16 K elements."""
+    return gemm_fp4(A, B, SFA, SFB, FP4_NV, add, rows, cols)
+
+
 def transpose_b16(X: np.ndarray) -> np.ndarray:
     """out[j, i] = X[i, j] on raw 16-bit patterns (plain double loop in C)."""
     X = np.asarray(X)
@@ -221,6 +295,7 @@ def transpose_b16(X: np.ndarray) -> np.ndarray:
 
 # Epilogue operation codes (the values of the library's C ABI, restated).
 EPI_NONE, EPI_ADD_SCALAR, EPI_SILU_AFFINE, EPI_BIAS_COL, EPI_BIAS_COL_SILU = 0, 1, 2, 3, 4
+EPI_AFFINE = 5
 
 
 def silu(x: np.ndarray) -> np.ndarray:
@@ -235,7 +310,8 @@ def apply_epilogue(ref: np.ndarray, op: int, alpha: float = 0.0, beta: float = 0
     """The fused epilogue on a float64 result block ``ref`` [rows, ncols].
 
     NONE: ref; ADD_SCALAR: ref + alpha; SILU_AFFINE: silu(ref) * alpha + beta;
-    BIAS_COL: ref + bias[j]; BIAS_COL_SILU: silu(ref + bias[j]).  ``bias`` is
+    BIAS_COL: ref + bias[j]; BIAS_COL_SILU: silu(ref + bias[j]);
+    AFFINE: ref * alpha + beta (e.g. a per-tensor scale of NVFP4 operands).  ``bias`` is
     the full per-column vector (length N); ``cols`` lists which columns the
     block holds (default: all, in order).
     """
@@ -246,6 +322,8 @@ def apply_epilogue(ref: np.ndarray, op: int, alpha: float = 0.0, beta: float = 0
         return ref + float(alpha)
     if op == EPI_SILU_AFFINE:
         return silu(ref) * float(alpha) + float(beta)
+    if op == EPI_AFFINE:
+        return ref * float(alpha) + float(beta)
     if op in (EPI_BIAS_COL, EPI_BIAS_COL_SILU):
         b = np.asarray(bias, dtype=np.float64)
         b = b if cols is None else b[np.asarray(cols)]

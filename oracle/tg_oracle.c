@@ -21,7 +21,8 @@
  *   - block scaling (".block_scale", "tcgen05.mma" section "Weight-stationary
  *     and block scaling") is taken in its plain MX reading: every element of
  *     A (resp. B) is multiplied by 2^(e - 127) where e is the E8M0 byte of
- *     its row and of its 32-element K block.
+ *     its row and of its 32-element K block; for FP4 (E2M1) operands the
+ *     scale is E8M0 per 32 elements (MXFP4) or UE4M3 per 16 (NVFP4).
  *
  * Parallelism: OpenMP over output rows only; each output keeps its own
  * ascending-k sum, so the thread count never changes a result.
@@ -85,6 +86,33 @@ double tgo_e8m0_to_f64(uint8_t bits)
 {
     if (bits == 0xFF) return NAN;
     return ldexp(1.0, (int)bits - 127);
+}
+
+/* FP4 E2M1 (OCP MX element format): 1 sign bit, 2 exponent bits (bias 1),
+ * 1 fraction bit, in the low 4 bits of `nibble`.  exponent 0: subnormal,
+ * value = f/2 * 2^0; otherwise (1 + f/2) * 2^(e-1).  No infinities or NaNs;
+ * the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double tgo_e2m1_to_f64(uint8_t nibble)
+{
+    int sign = (nibble >> 3) & 1;
+    int expo = (nibble >> 1) & 0x3;
+    int frac = nibble & 0x1;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac / 2.0, 0);
+    } else {
+        v = ldexp(1.0 + (double)frac / 2.0, expo - 1);
+    }
+    return sign ? -v : v;
+}
+
+/* UE4M3 scale (the unsigned use of E4M3 for NVFP4 block scales): the
+ * E4M3FN definition with the sign bit required to be 0; a set sign bit or
+ * the NaN code 0x7F decodes to NaN. */
+double tgo_ue4m3_to_f64(uint8_t bits)
+{
+    if (bits & 0x80) return NAN;
+    return tgo_e4m3fn_to_f64(bits);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -212,6 +240,69 @@ int tgo_gemm_mxfp8(const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
     return TGO_OK;
 }
 
+/*
+ * Block-scaled FP4 GEMM oracle ("tcgen05.mma", Block-scaled opcodes with
+ * .scale_vec::2X / ::4X).  A is [M, K/2] bytes (row stride lda bytes) of
+ * packed E2M1 values: element k of a row is the low nibble of byte k/2 when
+ * k is even and the high nibble when k is odd.  B is [N, K/2] likewise.
+ * scale_kind 0 (MXFP4): SFA is [M, K/32] E8M0 bytes, one per 32 consecutive
+ * K elements; scale_kind 1 (NVFP4): SFA is [M, K/16] UE4M3 bytes, one per 16.
+ * The decoded operand is a[i][k] = e2m1(A[i][k]) * scale(SFA[i][k / block]),
+ * likewise b; the product and the output selection are as in tgo_gemm_bf16.
+ */
+int tgo_gemm_fp4(const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+                 const uint8_t *SFA, int64_t ld_sfa, const uint8_t *SFB,
+                 int64_t ld_sfb, int64_t M, int64_t N, int64_t K, int scale_kind,
+                 double add, const int64_t *rows, int64_t nrows,
+                 const int64_t *cols, int64_t ncols, double *ref, double *mag)
+{
+    int64_t block;
+    if (scale_kind == 0) block = 32;
+    else if (scale_kind == 1) block = 16;
+    else return TGO_ERR_ARG;
+    if (!A || !B || !SFA || !SFB || !ref || !mag || M < 0 || N < 0 || K < 0)
+        return TGO_ERR_ARG;
+    if (K % block != 0 || 2 * lda < K || 2 * ldb < K || ld_sfa < K / block ||
+        ld_sfb < K / block)
+        return TGO_ERR_ARG;
+    if (!check_index_list(rows, nrows, M) || !check_index_list(cols, ncols, N))
+        return TGO_ERR_ARG;
+    if (!rows && nrows != M) return TGO_ERR_ARG;
+    if (!cols && ncols != N) return TGO_ERR_ARG;
+    if (nrows == 0 || ncols == 0) return TGO_OK;
+    if (K == 0) {
+        for (int64_t i = 0; i < nrows * ncols; ++i) { ref[i] = add; mag[i] = 0.0; }
+        return TGO_OK;
+    }
+    double *ad = (double *)malloc(sizeof(double) * (size_t)(nrows * K));
+    double *bd = (double *)malloc(sizeof(double) * (size_t)(ncols * K));
+    if (!ad || !bd) { free(ad); free(bd); return TGO_ERR_NOMEM; }
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = pick(rows, r);
+        for (int64_t k = 0; k < K; ++k) {
+            uint8_t byte = A[i * lda + k / 2];
+            uint8_t nib = (k % 2 == 0) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);
+            uint8_t sb = SFA[i * ld_sfa + k / block];
+            double sc = scale_kind == 0 ? tgo_e8m0_to_f64(sb) : tgo_ue4m3_to_f64(sb);
+            ad[r * K + k] = tgo_e2m1_to_f64(nib) * sc;
+        }
+    }
+    for (int64_t c = 0; c < ncols; ++c) {
+        int64_t j = pick(cols, c);
+        for (int64_t k = 0; k < K; ++k) {
+            uint8_t byte = B[j * ldb + k / 2];
+            uint8_t nib = (k % 2 == 0) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);
+            uint8_t sb = SFB[j * ld_sfb + k / block];
+            double sc = scale_kind == 0 ? tgo_e8m0_to_f64(sb) : tgo_ue4m3_to_f64(sb);
+            bd[c * K + k] = tgo_e2m1_to_f64(nib) * sc;
+        }
+    }
+    dot_grid(ad, bd, nrows, ncols, K, add, ref, mag);
+    free(ad);
+    free(bd);
+    return TGO_OK;
+}
+
 /* out[j][i] = in[i][j] on raw 16-bit patterns; in is [rows, cols] with row
  * stride ld_in, out is [cols, rows] with row stride ld_out. */
 int tgo_transpose_b16(const uint16_t *in, int64_t ld_in, uint16_t *out,
@@ -258,4 +349,14 @@ void tgo_decode_e4m3fn(const uint8_t *in, int64_t n, double *out)
 void tgo_decode_e8m0(const uint8_t *in, int64_t n, double *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = tgo_e8m0_to_f64(in[i]);
+}
+
+void tgo_decode_e2m1(const uint8_t *in, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = tgo_e2m1_to_f64(in[i]);
+}
+
+void tgo_decode_ue4m3(const uint8_t *in, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = tgo_ue4m3_to_f64(in[i]);
 }

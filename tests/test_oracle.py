@@ -272,6 +272,138 @@ def test_mxfp8_uniform_scale_is_power_of_two_factor(oracle):
 
 
 # ---------------------------------------------------------------------------
+# FP4 (E2M1) block-scaled products: .scale_vec::2X (MXFP4) and ::4X (NVFP4)
+# ---------------------------------------------------------------------------
+
+# The OCP MX E2M1 element table, code 0..15 (sign in bit 3).
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+              -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_all_codes(oracle):
+    v = oracle.decode_e2m1(np.arange(16, dtype=np.uint8))
+    assert list(v) == E2M1_TABLE
+    assert all(math.copysign(1, a) == math.copysign(1, b) for a, b in zip(v, E2M1_TABLE))
+    # only the low nibble is read
+    assert list(oracle.decode_e2m1(np.arange(16, dtype=np.uint8) | 0xA0)) == E2M1_TABLE
+
+
+def test_ue4m3_matches_torch_e4m3_for_positive_codes(oracle):
+    bits = np.arange(0, 0x7F, dtype=np.uint8)
+    assert np.array_equal(oracle.decode_ue4m3(bits), _e4m3_exact_via_torch(bits))
+    assert np.isnan(oracle.decode_ue4m3(np.array([0x7F, 0x80, 0xB8, 0xFF], np.uint8))).all()
+    assert list(oracle.decode_ue4m3(np.array([0x38, 0x40, 0x30, 0x7E], np.uint8))) == \
+        [1.0, 2.0, 0.5, 448.0]
+
+
+def test_e2m1_encoder_round_trip_and_ties(oracle):
+    codes = np.arange(16, dtype=np.uint8)
+    vals = np.array(E2M1_TABLE, dtype=np.float32)
+    assert np.array_equal(oracle.decode_e2m1(synth.f32_to_e2m1_codes(vals)), vals)
+    # midpoints round to the code with a zero fraction bit; beyond 6 saturates
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 9.0], dtype=np.float32)
+    assert list(oracle.decode_e2m1(synth.f32_to_e2m1_codes(mids))) == \
+        [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0]
+    packed = synth.pack_e2m1(codes.reshape(2, 8))
+    assert packed.shape == (2, 4) and packed[0, 0] == 0x10 and packed[1, 3] == 0xFE
+    assert np.array_equal(synth.unpack_e2m1(packed), codes.reshape(2, 8))
+
+
+def _unpack_python(packed, K):
+    """Element k of each row: low nibble of byte k // 2 for even k, else high."""
+    rows = []
+    for r in range(packed.shape[0]):
+        rows.append([(int(packed[r, k // 2]) >> (4 * (k % 2))) & 0xF for k in range(K)])
+    return rows
+
+
+@pytest.mark.parametrize("kind,block", [(0, 32), (1, 16)])
+def test_fp4_matches_exact_rationals(oracle, kind, block):
+    rng = np.random.default_rng(30 + kind)
+    M, N, K = 3, 4, 64
+    A = synth.e2m1_normal_packed(rng, (M, K))
+    B = synth.e2m1_normal_packed(rng, (N, K))
+    if kind == 0:
+        SFA, SFB = synth.e8m0_scales(rng, (M, K // 32)), synth.e8m0_scales(rng, (N, K // 32))
+        scale = lambda b: Fraction(2) ** (int(b) - 127)                       # noqa: E731
+    else:
+        SFA = synth.ue4m3_pow2_scales(rng, (M, K // 16))
+        SFB = np.array(rng.integers(0x20, 0x50, size=(N, K // 16)), np.uint8)   # any finite
+        lib = _e4m3_exact_via_torch(np.arange(256, dtype=np.uint8))
+        scale = lambda b: Fraction(float(lib[int(b)]))                       # noqa: E731
+    ref, mag = oracle.gemm_fp4(A, B, SFA, SFB, kind)
+    ua, ub = _unpack_python(A, K), _unpack_python(B, K)
+    for i in range(M):
+        for j in range(N):
+            terms = [Fraction(E2M1_TABLE[ua[i][k]]) * scale(SFA[i, k // block]) *
+                     Fraction(E2M1_TABLE[ub[j][k]]) * scale(SFB[j, k // block])
+                     for k in range(K)]
+            exact = sum(terms, Fraction(0))
+            emag = sum((abs(t) for t in terms), Fraction(0))
+            bound = Fraction(K * 2.0 ** -52 * float(emag))
+            assert abs(Fraction(ref[i, j]) - exact) <= bound
+            assert abs(Fraction(mag[i, j]) - emag) <= bound
+
+
+def test_fp4_unit_scales_equal_bf16_product(oracle):
+    rng = np.random.default_rng(32)
+    M, N, K = 9, 6, 128
+    A = synth.e2m1_normal_packed(rng, (M, K))
+    B = synth.e2m1_normal_packed(rng, (N, K))
+    table = np.array(E2M1_TABLE, dtype=np.float32)
+    # every E2M1 value is exact in bf16: decode with the table, not the oracle
+    Ab = synth.f32_to_bf16_bits(table[synth.unpack_e2m1(A)])
+    Bb = synth.f32_to_bf16_bits(table[synth.unpack_e2m1(B)])
+    want, wmag = oracle.gemm_bf16(Ab, Bb)
+    mx = oracle.gemm_mxfp4(A, B, np.full((M, K // 32), 127, np.uint8),
+                           np.full((N, K // 32), 127, np.uint8))
+    nv = oracle.gemm_nvfp4(A, B, np.full((M, K // 16), 0x38, np.uint8),
+                           np.full((N, K // 16), 0x38, np.uint8))
+    for ref, mag in (mx, nv):
+        assert np.array_equal(ref, want) and np.array_equal(mag, wmag)
+
+
+def test_fp4_nibble_order_one_hot(oracle):
+    # A row 0 holds 1.0 at element 1 only (high nibble of byte 0); B row j
+    # holds 2.0 at element j only.  Then D[0, j] = 2 for j == 1, else 0.
+    K = 32
+    A = np.zeros((1, K // 2), np.uint8)
+    A[0, 0] = 0x20
+    B = synth.pack_e2m1(np.eye(4, K, dtype=np.uint8) * 4)
+    ref, _ = oracle.gemm_mxfp4(A, B, np.full((1, 1), 127, np.uint8), np.full((4, 1), 127, np.uint8))
+    assert list(ref[0]) == [0.0, 2.0, 0.0, 0.0]
+
+
+@pytest.mark.parametrize("kind,block,two", [(0, 32, 128), (1, 16, 0x40)])
+def test_fp4_doubling_one_block_scale(oracle, kind, block, two):
+    rng = np.random.default_rng(33 + kind)
+    M, N, K = 5, 4, 128
+    A, B = synth.e2m1_normal_packed(rng, (M, K)), synth.e2m1_normal_packed(rng, (N, K))
+    one = 127 if kind == 0 else 0x38
+    SFA = np.full((M, K // block), one, np.uint8)
+    SFB = np.full((N, K // block), one, np.uint8)
+    base, _ = oracle.gemm_fp4(A, B, SFA, SFB, kind)
+    i, kb = 3, 1
+    codes = synth.unpack_e2m1(A)
+    only = np.zeros_like(codes)
+    only[i, block * kb:block * (kb + 1)] = codes[i, block * kb:block * (kb + 1)]
+    contrib, _ = oracle.gemm_fp4(synth.pack_e2m1(only), B, SFA, SFB, kind)
+    SFA2 = SFA.copy()
+    SFA2[i, kb] = two
+    raised, _ = oracle.gemm_fp4(A, B, SFA2, SFB, kind)
+    assert np.array_equal(raised, base + contrib)
+    assert np.array_equal(np.delete(raised, i, 0), np.delete(base, i, 0))
+
+
+def test_fp4_rejects_bad_shapes(oracle):
+    A = np.zeros((4, 16), np.uint8)
+    with pytest.raises(ValueError):
+        oracle.gemm_mxfp4(A, A, np.zeros((4, 2), np.uint8), np.zeros((4, 1), np.uint8))
+    with pytest.raises(ValueError):
+        oracle.gemm_nvfp4(A, A, np.zeros((4, 1), np.uint8), np.zeros((4, 1), np.uint8))
+
+
+# ---------------------------------------------------------------------------
 # data movement and layout models
 # ---------------------------------------------------------------------------
 
@@ -405,3 +537,9 @@ def test_epilogue_ops_closed_forms(oracle):
     # the add-one example is the ADD_SCALAR op with alpha = 1
     a = np.arange(768, dtype=np.float64).reshape(64, 12)
     assert np.array_equal(oracle.apply_epilogue(a, oracle.EPI_ADD_SCALAR, 1.0), a + 1)
+
+
+def test_epilogue_affine_closed_form(oracle):
+    ref = np.arange(12, dtype=np.float64).reshape(3, 4) - 5
+    out = oracle.apply_epilogue(ref, oracle.EPI_AFFINE, 0.25, -2.0)
+    assert np.array_equal(out, ref / 4 - 2)
