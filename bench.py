@@ -52,7 +52,8 @@ def workload() -> str:
 _CSRC = "blackwell_tile_gemm_gb300/csrc/"
 KERNEL_SOURCES = {
     "gemm": [_CSRC + f for f in ("gemm_kernel.cuh", "tg_ptx.cuh", "gemm_launch.cuh",
-                                 "gemm_bf16.cu", "gemm_mxfp8.cu")],
+                                 "gemm_kinds.h", "epilogue.cuh", "gemm_bf16.cu",
+                                 "gemm_blockscaled.cu")],
     "transpose": [_CSRC + f for f in ("transpose.cu", "tg_ptx.cuh")],
 }
 PROFILES = {
@@ -447,12 +448,13 @@ def run_configs(args):
             X = torch.from_numpy(x["X"].view(np.int16)).to(dev)
             out = torch.empty((w.N, w.M), dtype=torch.int16, device=dev)
             fn = lambda: tg.tile_transpose_b16(X, out)           # noqa: E731
-        elif w.kind == "mxfp8":
+        elif w.kind in ("mxfp8", "mxfp4", "nvfp4"):
             A, B, SFA, SFB = (torch.from_numpy(x[k]).to(dev) for k in ("A", "B", "SFA", "SFB"))
             D = torch.empty((w.M, w.N), device=dev,
                             dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
-            fn = lambda: tg.gemm_mxfp8_blockscaled(A, B, SFA, SFB, D, cta_pair=w.cta_pair,  # noqa
-                                                   **epi)
+            call = {"mxfp8": tg.gemm_mxfp8_blockscaled, "mxfp4": tg.gemm_mxfp4_blockscaled,
+                    "nvfp4": tg.gemm_nvfp4_blockscaled}[w.kind]
+            fn = lambda: call(A, B, SFA, SFB, D, cta_pair=w.cta_pair, **epi)  # noqa: E731
         else:
             A = torch.from_numpy(x["A"].view(np.int16)).to(dev).view(torch.bfloat16)
             B = torch.from_numpy(x["B"].view(np.int16)).to(dev).view(torch.bfloat16)
@@ -471,8 +473,13 @@ def run_configs(args):
             line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]))
         else:
             tf = w.flops / (ms * 1e-3) / 1e12
-            pk = float(peaks["bf16_tflops"]) * (2 if w.kind == "mxfp8" else 1)
+            # nominal dense ratios to bf16 (2.25 / 4.5 / 13.5 PFLOP/s per GPU)
+            ratio = {"mxfp8": 2, "mxfp4": 6, "nvfp4": 6}.get(w.kind, 1)
+            pk = float(peaks["bf16_tflops"]) * ratio
             line.update(tflops=tf, frac_of_cublas_bf16_burst_scaled=tf / pk)
+            if w.kind in ("mxfp4", "nvfp4"):
+                # the tensor-pipe rate the FP4 rate probe measures: 4x bf16 per clock
+                line["frac_of_probe_rate_4x_bf16"] = tf / (float(peaks["bf16_tflops"]) * 4)
         print(json.dumps(line), flush=True)
         del fn
         torch.cuda.empty_cache()

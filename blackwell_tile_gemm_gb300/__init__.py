@@ -36,6 +36,7 @@ TG_EPI_ADD_SCALAR = 1
 TG_EPI_SILU_AFFINE = 2
 TG_EPI_BIAS_COL = 3
 TG_EPI_BIAS_COL_SILU = 4
+TG_EPI_AFFINE = 5
 TG_FLAG_CTA_PAIR = 1
 TG_FLAG_MULTICAST = 2
 
@@ -84,6 +85,10 @@ def lib() -> ctypes.CDLL:
         L.gemm_mxfp8_blockscaled_ex.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                                 i64, i64, i64, i32, ctypes.POINTER(tg_epilogue),
                                                 u32, vp]
+        for name in ("gemm_mxfp4_blockscaled", "gemm_nvfp4_blockscaled"):
+            getattr(L, name).restype = i32
+            getattr(L, name).argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64,
+                                         i64, i32, ctypes.POINTER(tg_epilogue), u32, vp]
         L.gemm_mxfp8_blockscaled_noalloc.restype = i32
         L.gemm_mxfp8_blockscaled_noalloc.argtypes = list(L.gemm_mxfp8_blockscaled.argtypes)
         L.tile_transpose_b16.restype = i32
@@ -151,18 +156,24 @@ def _flags(cta_pair, multicast):
     return (TG_FLAG_CTA_PAIR if cta_pair else 0) | (TG_FLAG_MULTICAST if multicast else 0)
 
 
-def make_epilogue(epilogue_add=None, silu_affine=None, bias=None, bias_silu=False):
+def make_epilogue(epilogue_add=None, silu_affine=None, bias=None, bias_silu=False,
+                  affine=None):
     """Build the C epilogue description from keyword choices (at most one op).
 
     epilogue_add=s: D = acc + s;  silu_affine=(scale, shift): D = silu(acc) *
-    scale + shift;  bias=<f32 CUDA tensor [N]>: D = acc + bias[j], or with
-    bias_silu=True D = silu(acc + bias[j]).
+    scale + shift;  affine=(scale, shift): D = acc * scale + shift;
+    bias=<f32 CUDA tensor [N]>: D = acc + bias[j], or with bias_silu=True
+    D = silu(acc + bias[j]).
     """
-    chosen = [epilogue_add is not None, silu_affine is not None, bias is not None]
+    chosen = [epilogue_add is not None, silu_affine is not None, bias is not None,
+              affine is not None]
     if sum(chosen) > 1:
         raise ValueError("choose one epilogue")
     if epilogue_add is not None:
         return tg_epilogue(TG_EPI_ADD_SCALAR, float(epilogue_add), 0.0, None)
+    if affine is not None:
+        scale, shift = affine
+        return tg_epilogue(TG_EPI_AFFINE, float(scale), float(shift), None)
     if silu_affine is not None:
         scale, shift = silu_affine
         return tg_epilogue(TG_EPI_SILU_AFFINE, float(scale), float(shift), None)
@@ -176,7 +187,7 @@ def make_epilogue(epilogue_add=None, silu_affine=None, bias=None, bias_silu=Fals
 
 
 def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, silu_affine=None, bias=None,
-              bias_silu=False, cta_pair=False, multicast=False, stream=None):
+              bias_silu=False, affine=None, cta_pair=False, multicast=False, stream=None):
     """D[M,N] = A[M,K] @ B[N,K].T (+ epilogue_add), bf16 inputs, f32 accumulation.
 
     A, B: CUDA bfloat16 tensors with unit inner stride.  D: optional output
@@ -198,7 +209,7 @@ def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, silu_affine=No
         raise ValueError("D must be [M, N]")
     if bias is not None and bias.shape[0] != N:
         raise ValueError("bias must have N elements")
-    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu)
+    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu, affine)
     rc = lib().gemm_bf16_ex(A.data_ptr(), _ld(A, "A", 8), B.data_ptr(), _ld(B, "B", 8),
                             D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype),
                             ctypes.byref(epi), _flags(cta_pair, multicast), _stream_handle(stream))
@@ -207,8 +218,8 @@ def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, silu_affine=No
 
 
 def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_add=None,
-                           silu_affine=None, bias=None, bias_silu=False, cta_pair=False,
-                           multicast=False, stream=None):
+                           silu_affine=None, bias=None, bias_silu=False, affine=None,
+                           cta_pair=False, multicast=False, stream=None):
     """Block-scaled MXFP8 product: D = (A * 2^(SFA-127)) @ (B * 2^(SFB-127)).T.
 
     A: [M, K], B: [N, K] E4M3FN bytes (torch.float8_e4m3fn or uint8); SFA:
@@ -231,7 +242,7 @@ def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_a
         raise ValueError("D must be [M, N]")
     if bias is not None and bias.shape[0] != N:
         raise ValueError("bias must have N elements")
-    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu)
+    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu, affine)
     rc = lib().gemm_mxfp8_blockscaled_ex(
         A.data_ptr(), _ld(A, "A", 16), B.data_ptr(), _ld(B, "B", 16),
         SFA.data_ptr(), _ld(SFA, "SFA", 1), SFB.data_ptr(), _ld(SFB, "SFB", 1),
@@ -239,6 +250,62 @@ def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_a
         _flags(cta_pair, multicast), _stream_handle(stream))
     _check(rc, "gemm_mxfp8_blockscaled")
     return D
+
+
+def _gemm_fp4(fn_name, block, A, B, SFA, SFB, D, out_dtype, epi_kw, cta_pair, stream):
+    import torch
+    M, Kh = A.shape
+    N, Kh2 = B.shape
+    K = 2 * Kh
+    if Kh2 != Kh:
+        raise ValueError("A is [M, K/2] and B is [N, K/2] packed bytes")
+    for name, t in (("A", A), ("B", B), ("SFA", SFA), ("SFB", SFB)):
+        if t.element_size() != 1:
+            raise TypeError(f"{name} must hold 1-byte elements")
+    if tuple(SFA.shape) != (M, K // block) or tuple(SFB.shape) != (N, K // block):
+        raise ValueError(f"SFA must be [M, K/{block}] and SFB [N, K/{block}]")
+    if D is None:
+        D = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=A.device)
+    if tuple(D.shape) != (M, N):
+        raise ValueError("D must be [M, N]")
+    if epi_kw.get("bias") is not None and epi_kw["bias"].shape[0] != N:
+        raise ValueError("bias must have N elements")
+    epi = make_epilogue(**epi_kw)
+    rc = getattr(lib(), fn_name)(
+        A.data_ptr(), _ld(A, "A", 16), B.data_ptr(), _ld(B, "B", 16),
+        SFA.data_ptr(), _ld(SFA, "SFA", 1), SFB.data_ptr(), _ld(SFB, "SFB", 1),
+        D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype), ctypes.byref(epi),
+        _flags(cta_pair, False), _stream_handle(stream))
+    _check(rc, fn_name)
+    return D
+
+
+def gemm_mxfp4_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_add=None,
+                           silu_affine=None, bias=None, bias_silu=False, affine=None,
+                           cta_pair=False, stream=None):
+    """Block-scaled MXFP4 product: D = (a * 2^(SFA-127)) @ (b * 2^(SFB-127)).T.
+
+    A: [M, K/2], B: [N, K/2] uint8 of packed FP4 E2M1 (element 2i in the low
+    nibble of byte i); SFA: [M, K/32], SFB: [N, K/32] E8M0 bytes.  D float32
+    or bfloat16 (default bfloat16).  Epilogue keywords: see ``make_epilogue``.
+    """
+    return _gemm_fp4("gemm_mxfp4_blockscaled", 32, A, B, SFA, SFB, D, out_dtype,
+                     dict(epilogue_add=epilogue_add, silu_affine=silu_affine, bias=bias,
+                          bias_silu=bias_silu, affine=affine), cta_pair, stream)
+
+
+def gemm_nvfp4_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_add=None,
+                           silu_affine=None, bias=None, bias_silu=False, affine=None,
+                           cta_pair=False, stream=None):
+    """Block-scaled NVFP4 product: D = (a * ue4m3(SFA)) @ (b * ue4m3(SFB)).T.
+
+    A, B: packed E2M1 as for ``gemm_mxfp4_blockscaled``; SFA: [M, K/16],
+    SFB: [N, K/16] UE4M3 bytes (sign bit clear).  A per-tensor scale goes in
+    ``affine=(scale, 0.0)``.
+    """
+    return _gemm_fp4("gemm_nvfp4_blockscaled", 16, A, B, SFA, SFB, D, out_dtype,
+                     dict(epilogue_add=epilogue_add, silu_affine=silu_affine, bias=bias,
+                          bias_silu=bias_silu, affine=affine), cta_pair, stream)
 
 
 def gemm_mxfp8_blockscaled_noalloc(A, B, SFA, SFB, D, *, epilogue_add=None, cta_pair=False,

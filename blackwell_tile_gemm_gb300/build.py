@@ -19,9 +19,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtgemm.so")
-SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_mxfp8.cu", "gemm_mxfp8_noalloc.cu",
-           "transpose.cu", "probes.cu"]
-HEADERS = ["tg_ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh", "tg_internal.h", "epilogue.cuh"]
+SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_blockscaled.cu", "gemm_fp4.cu",
+           "gemm_mxfp8_noalloc.cu", "transpose.cu", "probes.cu"]
+HEADERS = ["tg_ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh", "tg_internal.h", "epilogue.cuh",
+           "gemm_kinds.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

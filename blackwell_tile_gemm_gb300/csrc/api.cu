@@ -141,28 +141,30 @@ void* device_workspace(size_t bytes) {
   return p;
 }
 
-int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
+int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,
                 const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D,
                 int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, const Epi& epi,
                 unsigned flags, cudaStream_t stream, DeviceCtx* ctx) {
   if (K == 0) return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi, stream);
   const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
   const bool mcast = (flags & TG_FLAG_MULTICAST) != 0;
-  if (!mx)
+  if (kind == kKindBf16)
     return launch_gemm_bf16_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M),
                                  static_cast<int>(N), static_cast<int>(K), d_dtype, epi, pair,
                                  mcast, stream, ctx);
-  uint8_t* ws = static_cast<uint8_t*>(device_workspace(mxfp8_workspace_bytes(M, N, K, pair)));
+  uint8_t* ws = static_cast<uint8_t*>(
+      device_workspace(blockscaled_workspace_bytes(kind, M, N, K, pair)));
   if (ws == nullptr) return TG_ERR_CUDA;
-  return launch_gemm_mxfp8_impl(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
-                                static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                d_dtype, epi, pair, mcast, ws, stream, ctx);
+  return launch_gemm_blockscaled_impl(kind, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
+                                      static_cast<int>(M), static_cast<int>(N),
+                                      static_cast<int>(K), d_dtype, epi, pair, mcast, ws,
+                                      stream, ctx);
 }
 
 int check_epilogue(const tg_epilogue* epi, Epi* out) {
   Epi e{kEpiNone, 0.0f, 0.0f, nullptr};
   if (epi != nullptr) {
-    if (epi->op < kEpiNone || epi->op > kEpiBiasColSilu) return TG_ERR_INVALID_ARG;
+    if (epi->op < kEpiNone || epi->op > kEpiAffine) return TG_ERR_INVALID_ARG;
     e.op = epi->op;
     e.alpha = epi->alpha;
     e.beta = epi->beta;
@@ -184,9 +186,11 @@ namespace {
 
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 
+// a_esize: bytes per ld unit of A and B; k_per_unit: K elements per ld unit
+// (2 for packed FP4, whose rows are K / 2 bytes).
 int check_gemm_common(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
                       int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
-                      unsigned flags, int a_esize) {
+                      unsigned flags, int a_esize, int k_per_unit = 1) {
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return TG_ERR_INVALID_ARG;
   if (d_dtype != TG_D_F32 && d_dtype != TG_D_BF16) return TG_ERR_INVALID_ARG;
@@ -199,7 +203,8 @@ int check_gemm_common(const void* A, int64_t lda, const void* B, int64_t ldb, vo
   const int d_esize = d_dtype == TG_D_F32 ? 4 : 2;
   if (!aligned16(D) || (ldd * d_esize) % 16 != 0) return TG_ERR_MISALIGNED;
   if (K == 0) return TG_OK;
-  if (A == nullptr || B == nullptr || lda < K || ldb < K) return TG_ERR_INVALID_ARG;
+  if (A == nullptr || B == nullptr || lda * k_per_unit < K || ldb * k_per_unit < K)
+    return TG_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B)) return TG_ERR_MISALIGNED;
   if ((lda * a_esize) % 16 != 0 || (ldb * a_esize) % 16 != 0) return TG_ERR_MISALIGNED;
   return TG_OK;
@@ -213,14 +218,20 @@ namespace tg {
 
 // Argument checks of the block-scaled call, shared with the variant that
 // takes its scratch from a static array (gemm_mxfp8_noalloc.cu).
-int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb, const void* SFA,
-                     int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D, int64_t ldd,
-                     int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
-                     unsigned flags) {
-  if (K % 32 != 0) return TG_ERR_INVALID_ARG;
-  int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 1);
+int check_blockscaled_args(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           int epilogue, unsigned flags) {
+  if (kind != kKindMxf8 && kind != kKindMxf4 && kind != kKindNvf4) return TG_ERR_INVALID_ARG;
+  const int block = scale_block_of(kind);
+  if (K % block != 0) return TG_ERR_INVALID_ARG;
+  // Multicast clusters exist for MXFP8 only.
+  if (kind != kKindMxf8 && (flags & TG_FLAG_MULTICAST) && (flags & TG_FLAG_CTA_PAIR))
+    return TG_ERR_UNSUPPORTED;
+  int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 1,
+                             kind == kKindMxf8 ? 1 : 2);
   if (rc != TG_OK || M == 0 || N == 0) return rc;
-  if (K > 0 && (SFA == nullptr || SFB == nullptr || ld_sfa < K / 32 || ld_sfb < K / 32))
+  if (K > 0 && (SFA == nullptr || SFB == nullptr || ld_sfa < K / block || ld_sfb < K / block))
     return TG_ERR_INVALID_ARG;
   return TG_OK;
 }
@@ -239,8 +250,8 @@ int gemm_bf16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, void* D
   if (rc != TG_OK || M == 0 || N == 0) return rc;
   DeviceCtx* ctx = current_ctx();
   if (!ctx) return TG_ERR_CUDA;
-  return launch_gemm(false, A, lda, B, ldb, nullptr, 0, nullptr, 0, D, ldd, M, N, K, d_dtype, e,
-                     flags, as_stream(cuda_stream), ctx);
+  return launch_gemm(kKindBf16, A, lda, B, ldb, nullptr, 0, nullptr, 0, D, ldd, M, N, K,
+                     d_dtype, e, flags, as_stream(cuda_stream), ctx);
 }
 
 int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
@@ -264,8 +275,8 @@ int gemm_mxfp8_blockscaled_ex(const void* A, int64_t lda, const void* B, int64_t
   if (rc != TG_OK || M == 0 || N == 0) return rc;
   DeviceCtx* ctx = current_ctx();
   if (!ctx) return TG_ERR_CUDA;
-  return launch_gemm(true, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K, d_dtype, e,
-                     flags, as_stream(cuda_stream), ctx);
+  return launch_gemm(kKindMxf8, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K,
+                     d_dtype, e, flags, as_stream(cuda_stream), ctx);
 }
 
 int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
@@ -276,6 +287,46 @@ int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ld
   const tg_epilogue e{epilogue, epi_scalar, 0.0f, nullptr};
   return gemm_mxfp8_blockscaled_ex(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K,
                                    d_dtype, &e, flags, cuda_stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int gemm_fp4_common(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,
+                    const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D,
+                    int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                    const tg_epilogue* epi, unsigned flags, void* cuda_stream) {
+  Epi e;
+  int rc = check_epilogue(epi, &e);
+  if (rc != TG_OK) return rc;
+  rc = check_blockscaled_args(kind, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K,
+                              d_dtype, TG_EPI_NONE, flags);
+  if (rc != TG_OK || M == 0 || N == 0) return rc;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  return launch_gemm(kind, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K, d_dtype, e,
+                     flags, as_stream(cuda_stream), ctx);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_mxfp4_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           const tg_epilogue* epi, unsigned flags, void* cuda_stream) {
+  return gemm_fp4_common(kKindMxf4, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K,
+                         d_dtype, epi, flags, cuda_stream);
+}
+
+int gemm_nvfp4_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           const tg_epilogue* epi, unsigned flags, void* cuda_stream) {
+  return gemm_fp4_common(kKindNvf4, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M, N, K,
+                         d_dtype, epi, flags, cuda_stream);
 }
 
 int tile_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out, int64_t rows,

@@ -3,7 +3,8 @@
 // before the conversion to D's type.  It follows "Explicit CUDA tile
 // patterns", section "Scalar compositions" (TVM TIRx): a caller-chosen scalar
 // function such as silu_affine(x, scale, bias) = x / (1 + exp(-x)) * scale +
-// bias, inlined at each register element.
+// bias, inlined at each register element.  AFFINE (x * alpha + beta) carries
+// a per-tensor scale, e.g. the global scale of NVFP4 operands.
 #pragma once
 
 #include <cstdint>
@@ -24,6 +25,7 @@ enum : int {
   kEpiSiluAffine = 2,
   kEpiBiasCol = 3,
   kEpiBiasColSilu = 4,
+  kEpiAffine = 5,
 };
 
 __host__ __device__ constexpr bool epi_uses_bias(int op) {
@@ -40,11 +42,12 @@ __device__ __forceinline__ float silu_f32(float x) {
 }
 
 // The ops other than NONE / ADD_SCALAR, on one value; `b` is the column's
-// bias (unused by SILU_AFFINE).  NONE and ADD_SCALAR are applied by the
+// bias (unused by SILU_AFFINE and AFFINE).  NONE and ADD_SCALAR are applied by the
 // stores themselves, as acc + (0 or alpha).
 __device__ __forceinline__ float apply_epi_general(int op, float alpha, float beta, float x,
                                                    float b) {
   if (op == kEpiSiluAffine) return silu_f32(x) * alpha + beta;
+  if (op == kEpiAffine) return x * alpha + beta;
   if (op == kEpiBiasCol) return x + b;
   return silu_f32(x + b);
 }

@@ -15,13 +15,13 @@ namespace tg {
 namespace {
 // m-tiles per band of the persistent tile order.
 constexpr int kRasterGroup = 8;
-using CfgF32 = GemmCfg<1, false, 256, 2, 4, false>;
-using CfgBf16 = GemmCfg<1, false, 256, 2, 4, true>;
-using CfgPairF32 = GemmCfg<2, false, 256, 2, 6, false>;
-using CfgPairBf16 = GemmCfg<2, false, 256, 2, 6, true>;
+using CfgF32 = GemmCfg<1, kKindBf16, 256, 2, 4, false>;
+using CfgBf16 = GemmCfg<1, kKindBf16, 256, 2, 4, true>;
+using CfgPairF32 = GemmCfg<2, kKindBf16, 256, 2, 6, false>;
+using CfgPairBf16 = GemmCfg<2, kKindBf16, 256, 2, 6, true>;
 // Clusters of two CTA pairs multicasting the shared B tile (TG_FLAG_MULTICAST).
-using CfgPairMcF32 = GemmCfg<2, false, 256, 2, 6, false, true>;
-using CfgPairMcBf16 = GemmCfg<2, false, 256, 2, 6, true, true>;
+using CfgPairMcF32 = GemmCfg<2, kKindBf16, 256, 2, 6, false, true>;
+using CfgPairMcBf16 = GemmCfg<2, kKindBf16, 256, 2, 6, true, true>;
 }  // namespace
 
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,

@@ -13,14 +13,19 @@
 //
 //   warp 0      TMA producer: one lane waits for a free ring slot, posts the
 //               expected bytes and issues the A / B (and scale-image) loads.
-//   warp 1      TMEM allocator and MMA issuer: one lane waits for a full slot,
-//               (copies the scale images into TMEM,) issues the K16 / K32
-//               MMAs, and commits to the slot's "empty" barrier; at the end of
-//               a tile it commits to the accumulator's "full" barrier.
+//   warp 1      TMEM allocator and MMA issuer: one lane waits for a full slot
+//               (block-scaled: for its scales in TMEM), issues the four MMAs
+//               of 32 bytes of K each, and commits to the slot's "empty"
+//               barrier; at the end of a tile it commits to the accumulator's
+//               "full" barrier.
 //   warps 2..9  epilogue: wait for a full accumulator; each warp reads its
 //               32 TMEM lanes x BN/2 columns with tcgen05.ld (row = lane) into
 //               registers and releases the accumulator at once, then applies
 //               the scalar op, converts and stores with st.global.v4.
+//   warps 10,11 block-scaled kinds only: scale copiers; once a stage's data
+//               has landed, each copies half of its scale images into the
+//               stage's TMEM scale columns (tcgen05.cp) and commits to the
+//               stage's "scales ready" barrier, which the MMAs wait for.
 //
 // Tiles are visited persistently (one CTA or CTA pair per SM, static stride)
 // in grouped order so that CTAs running at the same time share A and B panels
@@ -58,7 +63,9 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-template <int kCtaGroup_, bool kMx_, int kBN_, int kAccBufs_, int kStages_, bool kBf16Out_,
+// kKind_: kKindBf16 (dense bf16) or one of the block-scaled kinds kKindMxf8,
+// kKindMxf4, kKindNvf4 (tg_ptx.cuh).
+template <int kCtaGroup_, int kKind_, int kBN_, int kAccBufs_, int kStages_, bool kBf16Out_,
           bool kMcast_ = false>
 struct GemmCfg {
   static constexpr int kCtaGroup = kCtaGroup_;
@@ -68,21 +75,29 @@ struct GemmCfg {
   static constexpr bool kMcast = kMcast_;
   static constexpr int kPairs = kMcast ? 2 : 1;           // MMA units per cluster
   static constexpr int kClusterCtas = kCtaGroup * kPairs;
-  static constexpr bool kMx = kMx_;
+  static constexpr int kKind = kKind_;
+  static constexpr bool kMx = kKind != kKindBf16;   // block-scaled
+  // Scale layout per stage (128 bytes of K per row = 4 MMAs of 32 bytes):
+  // an MMA reads kSfVec scales per row, so a stage needs kSfVec 512-byte
+  // images of 128 rows x 4 scale bytes per 128-row block.
+  static constexpr int kSfVec = scale_vec_of(kKind);
+  static constexpr int kSfGroups = kSfVec;
   static constexpr int BM = 128;                    // D rows per CTA (TMEM lanes)
   static constexpr int BN = kBN_;                   // D columns per tile (MMA N)
   static constexpr int kAccBufs = kAccBufs_;
   static constexpr int kStages = kStages_;
   static constexpr bool kBf16Out = kBf16Out_;
-  static constexpr int BK = kMx ? 128 : 64;         // K elements per stage = 128 bytes
-  static constexpr int UMMA_K = kMx ? 32 : 16;      // K elements per MMA issue = 32 bytes
-  static constexpr int kIssues = BK / UMMA_K;       // 4 issues per stage
+  // Tensor-map elements per stage along K (128 bytes: 64 bf16 or 128 one-byte
+  // elements; a packed-FP4 map is addressed in bytes, 2 values each).
+  static constexpr int BK = kMx ? 128 : 64;
+  static constexpr int kIssues = 4;                 // MMAs of 32 bytes of K per stage
   static constexpr int B_ROWS = BN / kCtaGroup;     // B rows this CTA stages
   static constexpr int B_LOAD_ROWS = B_ROWS / kPairs;  // B rows this CTA loads
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = B_ROWS * 128;
-  static constexpr int SFA_BYTES = kMx ? 512 : 0;   // 128 rows x 4 K-blocks
-  static constexpr int SFB_BYTES = kMx ? (BN / 128) * 512 : 0;
+  static constexpr int kSfBlocksB = BN / 128;       // 128-row blocks of SFB per tile
+  static constexpr int SFA_BYTES = kSfGroups * 512;
+  static constexpr int SFB_BYTES = kSfGroups * kSfBlocksB * 512;
   static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
@@ -90,14 +105,21 @@ struct GemmCfg {
   static constexpr int OFF_SFA = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + kStages * SFA_BYTES;
   static constexpr int OFF_BAR = (OFF_SFB + kStages * SFB_BYTES + 7) & ~7;
+  // Block-scaled kinds: two warps copy the scales into TMEM, each issuing
+  // half of a stage's tcgen05.cp.  A copy costs its issuing thread ~80
+  // cycles before the next one issues, while copies from different warps
+  // proceed in parallel, and none of them delays MMAs issued by another warp;
+  // so the copies leave the MMA thread, and two issuers keep up with the 12
+  // copies an NVFP4 stage needs within the 512 cycles of its MMAs.
+  static constexpr int kSfWarps = kMx ? 2 : 0;
   static constexpr int NUM_BARS =
-      (kMx && kCtaGroup == 2 ? 3 : 2) * kStages + 2 * kAccBufs + (kMx && kCtaGroup == 2 ? 2 : 1);
+      (kMx ? 3 : 2) * kStages + 2 * kAccBufs + 1 + kSfWarps;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   // tensor memory columns
   static constexpr int ACC_COLS = BN;
-  static constexpr int SFA_COLS = kMx ? 4 : 0;
-  static constexpr int SFB_COLS = kMx ? BN / 32 : 0;
+  static constexpr int SFA_COLS = 4 * kSfGroups;
+  static constexpr int SFB_COLS = 4 * kSfGroups * kSfBlocksB;
   static constexpr int SF_COL0 = ACC_COLS * kAccBufs;
   static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
   static constexpr int TMEM_USED = SF_COL0 + SF_STAGE_COLS * kStages;
@@ -112,16 +134,14 @@ struct GemmCfg {
   static constexpr int kEpiWarps = 8;
   static constexpr int kEpiCols = BN / 2;
   static constexpr int kEpiChunks = kEpiCols / 32;
-  // Block-scaled CTA pairs: a separate warp copies the scales into TMEM so
-  // that the copies overlap the MMAs instead of queueing in front of them.
-  static constexpr bool kSfWarp = kMx && kCtaGroup == 2;
-  static constexpr int kSfWarpId = 2 + kEpiWarps;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps + (kSfWarp ? 32 : 0);
+  static constexpr int kSfWarp0 = 2 + kEpiWarps;    // first scale-copy warp
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kSfWarps;
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(!kMcast || kCtaGroup == 2, "multicast clusters are made of CTA pairs");
+  static_assert(!kMx || BN % 128 == 0, "scale images cover 128-row blocks of B");
 };
 
 // Grouped tile order: consecutive tile ids walk down a band of `group`
@@ -138,6 +158,34 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   tn = r / gm;
 }
 
+// Copies one stage's scale images from shared memory into its TMEM scale
+// columns (32 rows x 16 bytes per copy, replicated into the four 32-lane
+// slabs; 8-row groups 128 bytes apart).  Shared layout per stage: SFA
+// [group][512 B], SFB [block][group][512 B].  TMEM layout from column sfa_t:
+// SFA group g at 4g; SFB group g, block b at SFA_COLS + 4 (g * blocks + b),
+// so that the blocks of one group are adjacent columns, as an MMA of N = BN
+// reads them (row r of SFB in byte column 4 (r / 32) + sf).
+// The copies are numbered SFA images first, then SFB (block, image); copier
+// `part` of kSfWarps issues those whose number is part modulo kSfWarps.
+template <class C>
+__device__ __forceinline__ void copy_stage_scales(uint32_t sfa_t, uint64_t sfadesc0,
+                                                  uint64_t sfbdesc0, int stage, int part) {
+#pragma unroll
+  for (int g = 0; g < C::kSfGroups; ++g)
+    if (g % C::kSfWarps == part)
+      tmem_cp_32x128b_warpx4<C::kCtaGroup>(
+          sfa_t + 4 * g, sfadesc0 + static_cast<uint64_t>((stage * C::SFA_BYTES + 512 * g) >> 4));
+#pragma unroll
+  for (int b = 0; b < C::kSfBlocksB; ++b)
+#pragma unroll
+    for (int g = 0; g < C::kSfGroups; ++g)
+      if ((C::kSfGroups + b * C::kSfGroups + g) % C::kSfWarps == part)
+        tmem_cp_32x128b_warpx4<C::kCtaGroup>(
+            sfa_t + C::SFA_COLS + 4 * (g * C::kSfBlocksB + b),
+            sfbdesc0 + static_cast<uint64_t>(
+                           (stage * C::SFB_BYTES + 512 * (b * C::kSfGroups + g)) >> 4));
+}
+
 // Four column biases starting at `c` (zeros past N).
 __device__ __forceinline__ float4 bias4(const GemmArgs& p, int c) {
   if (c + 4 <= p.N) {
@@ -151,13 +199,20 @@ __device__ __forceinline__ float4 bias4(const GemmArgs& p, int c) {
   return make_float4(t[0], t[1], t[2], t[3]);
 }
 
-// SILU_AFFINE / BIAS_COL / BIAS_COL_SILU on 32 accumulator columns
+// SILU_AFFINE / AFFINE / BIAS_COL / BIAS_COL_SILU on 32 accumulator columns
 // [col0, col0+32) of one row, in place.  The op is uniform over the launch,
 // so each branch below runs without divergence.
 __device__ __forceinline__ void epilogue_general_chunk(const GemmArgs& p, int col0,
                                                        uint32_t (&v)[32]) {
   const int op = p.epi.op;
   const float alpha = p.epi.alpha, beta = p.epi.beta;
+  if (op == kEpiAffine) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      v[i] = __float_as_uint(apply_epi_general(kEpiAffine, alpha, beta,
+                                               __uint_as_float(v[i]), 0.0f));
+    return;
+  }
   if (op == kEpiSiluAffine) {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
@@ -251,7 +306,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t* acce_bar = accf_bar + C::kAccBufs;        // [kAccBufs] epilogue -> MMA
   uint64_t* drain_bar = acce_bar + C::kAccBufs;       // MMA completion on give-up
   uint64_t* sfr_bar = drain_bar + 1;                  // [kStages] scales in TMEM -> MMA
-  uint64_t* sf_drain_bar = sfr_bar + C::kStages;      // scale copies on give-up
+  uint64_t* sf_drain_bar = sfr_bar + C::kStages;      // [kSfWarps] copies on give-up
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -277,9 +332,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&acce_bar[b], C::kEpiWarps * C::kCtaGroup);
     }
     mbar_init(drain_bar, 1);
-    if constexpr (C::kSfWarp) {
-      for (int s = 0; s < C::kStages; ++s) mbar_init(&sfr_bar[s], 1);
-      mbar_init(sf_drain_bar, 1);
+    if constexpr (C::kMx) {
+      for (int s = 0; s < C::kStages; ++s) mbar_init(&sfr_bar[s], C::kSfWarps);
+      for (int w = 0; w < C::kSfWarps; ++w) mbar_init(&sf_drain_bar[w], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -399,16 +454,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (lane == 0 && leader) {
       const uint32_t acce0 = smem_addr(&acce_bar[0]);
       // K-major, 128-byte swizzled operands: 8-row groups 1024 bytes apart;
-      // the K16 / K32 slice k of a stage starts 32 * k bytes into each row.
+      // MMA k of a stage reads the 32-byte K slice k of each row.
       const uint64_t adesc0 =
           make_smem_desc(smem_addr(smem + C::OFF_A), 16, 1024, kDescSwizzle128B);
       const uint64_t bdesc0 =
           make_smem_desc(smem_addr(smem + C::OFF_B), 16, 1024, kDescSwizzle128B);
-      // Scale images: 32 rows x 16 bytes per tcgen05.cp, 8-row groups 128 bytes apart.
-      const uint64_t sfadesc0 =
-          make_smem_desc(smem_addr(smem + C::OFF_SFA), 16, 128, kDescSwizzleNone);
-      const uint64_t sfbdesc0 =
-          make_smem_desc(smem_addr(smem + C::OFF_SFB), 16, 128, kDescSwizzleNone);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -417,7 +467,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       bool ready = false;       // ready barrier of `stage` already seen complete
       // The MMAs of a stage wait for its TMA data, or with a scale warp for
       // its scales in TMEM (which that warp copies after the data landed).
-      uint64_t* ready_bar = C::kSfWarp ? sfr_bar : full_bar;
+      uint64_t* ready_bar = C::kMx ? sfr_bar : full_bar;
       const uint32_t ready0 = smem_addr(&ready_bar[0]);
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         if (!mbar_try_wait(acce0 + 8u * acc, acc_phase ^ 1u) &&
@@ -441,21 +491,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if constexpr (C::kMx) {
             const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_STAGE_COLS;
             const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-            if constexpr (!C::kSfWarp) {
-              // Scales go to this stage's TMEM columns before the MMAs read them.
-              tmem_cp_32x128b_warpx4<C::kCtaGroup>(
-                  sfa_t, sfadesc0 + static_cast<uint64_t>(stage * (C::SFA_BYTES >> 4)));
-#pragma unroll
-              for (int j = 0; j < C::BN / 128; ++j)
-                tmem_cp_32x128b_warpx4<C::kCtaGroup>(
-                    sfb_t + 4 * j,
-                    sfbdesc0 + static_cast<uint64_t>(stage * (C::SFB_BYTES >> 4) + 32 * j));
-            }
 #pragma unroll
             for (int k = 0; k < C::kIssues; ++k) {
-              mma_mxf8<C::kCtaGroup>(d_tmem, ad + 2 * k, bd + 2 * k,
-                                     idesc_mxf8_e4m3(C::MMA_M, C::BN, k, k), sfa_t, sfb_t,
-                                     (kb | k) != 0);
+              // MMA k reads kSfVec scales per row starting at scale k * kSfVec
+              // of the stage: image g, byte offset (scale-factor id) sf.
+              const int g = (k * C::kSfVec) / 4, sf = (k * C::kSfVec) % 4;
+              mma_block_scaled<C::kCtaGroup, C::kKind>(
+                  d_tmem, ad + 2 * k, bd + 2 * k,
+                  idesc_block_scaled<C::kKind>(C::MMA_M, C::BN, sf, sf), sfa_t + 4 * g,
+                  sfb_t + 4 * g * C::kSfBlocksB, (kb | k) != 0);
               if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           } else {
@@ -493,9 +537,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mbar_wait_drain(drain_bar, 0, p.timeout_ns);
       }
     }
-  } else if (C::kSfWarp && warp == C::kSfWarpId) {
-    // ------------------------------------------------------------ scale copier
-    if constexpr (C::kSfWarp) {
+  } else if (C::kMx && warp >= C::kSfWarp0 && warp < C::kSfWarp0 + C::kSfWarps) {
+    // ------------------------------------------------------------ scale copiers
+    if constexpr (C::kMx) {
+      const int part = warp - C::kSfWarp0;
       if (lane == 0 && leader) {
         const uint64_t sfadesc0 =
             make_smem_desc(smem_addr(smem + C::OFF_SFA), 16, 128, kDescSwizzleNone);
@@ -514,16 +559,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               break;
             }
             tc_fence_after_sync();
-            // 32 rows x 16 bytes per copy, 8-row groups 128 bytes apart.
-            const uint32_t tcol = tmem_base + C::SF_COL0 + stage * C::SF_STAGE_COLS;
-            tmem_cp_32x128b_warpx4<C::kCtaGroup>(
-                tcol, sfadesc0 + static_cast<uint64_t>(stage * (C::SFA_BYTES >> 4)));
-#pragma unroll
-            for (int j = 0; j < C::BN / 128; ++j)
-              tmem_cp_32x128b_warpx4<C::kCtaGroup>(
-                  tcol + C::SFA_COLS + 4 * j,
-                  sfbdesc0 + static_cast<uint64_t>(stage * (C::SFB_BYTES >> 4) + 32 * j));
-            mma_commit_pair(&sfr_bar[stage], static_cast<uint16_t>(1u << lead_rank));
+            copy_stage_scales<C>(tmem_base + C::SF_COL0 + stage * C::SF_STAGE_COLS, sfadesc0,
+                                 sfbdesc0, stage, part);
+            if constexpr (C::kCtaGroup == 1)
+              mma_commit(&sfr_bar[stage]);
+            else
+              mma_commit_pair(&sfr_bar[stage], static_cast<uint16_t>(1u << lead_rank));
             copied = true;
             if (++stage == C::kStages) {
               stage = 0;
@@ -533,8 +574,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         if (copied && (!ok || *abort_flag)) {
           // Gave up: the copies already issued finish before TMEM is freed.
-          mma_commit_pair(sf_drain_bar, static_cast<uint16_t>(1u << lead_rank));
-          mbar_wait_drain(sf_drain_bar, 0, p.timeout_ns);
+          if constexpr (C::kCtaGroup == 1)
+            mma_commit(&sf_drain_bar[part]);
+          else
+            mma_commit_pair(&sf_drain_bar[part], static_cast<uint16_t>(1u << lead_rank));
+          mbar_wait_drain(&sf_drain_bar[part], 0, p.timeout_ns);
         }
       }
     }

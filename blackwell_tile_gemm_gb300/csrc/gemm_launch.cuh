@@ -80,4 +80,11 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
 
 inline int ceil_div_i(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// Launches the FP4 configuration of `kind` (kKindMxf4 / kKindNvf4) with the
+// tensor maps and arguments the shared block-scaled plan built
+// (gemm_fp4.cu).  Multicast clusters are not built for FP4.
+int launch_gemm_fp4_cfg(int kind, bool pair, bool bf16_out, const CUtensorMap& tA,
+                        const CUtensorMap& tB, const CUtensorMap& tSA, const CUtensorMap& tSB,
+                        const GemmArgs& a, cudaStream_t stream, DeviceCtx* ctx);
+
 }  // namespace tg

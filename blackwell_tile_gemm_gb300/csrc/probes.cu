@@ -250,10 +250,12 @@ __global__ void __launch_bounds__(128) mma_rate_kernel(int iters, unsigned long 
   }
   // Small integers (0x3C00 pattern = 1.0 in bf16 pairs / 1.5 in E4M3 pairs),
   // unit scales: no denormals, no NaNs.
+  // FP4 kinds: nibbles 0x2 = 1.0; NVFP4 scales UE4M3 0x38 = 1.0.
   for (int i = tid; i < (128 + 256) * 128 / 4; i += blockDim.x)
-    reinterpret_cast<uint32_t*>(sa)[i] = kKind == 0 ? 0x3F803F80u : 0x38383838u;
+    reinterpret_cast<uint32_t*>(sa)[i] =
+        kKind == 0 ? 0x3F803F80u : kKind >= 3 ? 0x22222222u : 0x38383838u;
   for (int i = tid; i < 3 * 512 / 4; i += blockDim.x)
-    reinterpret_cast<uint32_t*>(ssf)[i] = 0x7F7F7F7Fu;
+    reinterpret_cast<uint32_t*>(ssf)[i] = kKind == 4 ? 0x38383838u : 0x7F7F7F7Fu;
   fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(128) mma_rate_kernel(int iters, unsigned long 
   if (tid == 0) {
     const uint32_t a0 = smem_addr(sa), b0 = smem_addr(sb), f0 = smem_addr(ssf);
     const uint32_t sfa = tmem + 256, sfb = tmem + 260;
-    if constexpr (kKind == 1) {
+    if constexpr (kKind == 1 || kKind >= 3) {
       tmem_cp_32x128b_warpx4<1>(sfa, make_smem_desc(f0, 16, 128, kDescSwizzleNone));
       tmem_cp_32x128b_warpx4<1>(sfb, make_smem_desc(f0 + 512, 16, 128, kDescSwizzleNone));
       tmem_cp_32x128b_warpx4<1>(sfb + 4, make_smem_desc(f0 + 1024, 16, 128, kDescSwizzleNone));
@@ -279,8 +281,17 @@ __global__ void __launch_bounds__(128) mma_rate_kernel(int iters, unsigned long 
           mma_bf16<1>(tmem, ad, bd, idesc_bf16_f32(128, 256), (it | k) != 0);
         else if constexpr (kKind == 1)
           mma_mxf8<1>(tmem, ad, bd, idesc_mxf8_e4m3(128, 256, k, k), sfa, sfb, (it | k) != 0);
-        else
+        else if constexpr (kKind == 2)
           mma_f8_dense(tmem, ad, bd, idesc_f8_e4m3_f32(128, 256), (it | k) != 0);
+        else if constexpr (kKind == 3)   // MXFP4: scale ids 0 / 2 of one column
+          mma_block_scaled<1, kKindMxf4>(tmem, ad, bd,
+                                         idesc_block_scaled<kKindMxf4>(128, 256, 2 * (k & 1),
+                                                                       2 * (k & 1)),
+                                         sfa, sfb, (it | k) != 0);
+        else
+          mma_block_scaled<1, kKindNvf4>(tmem, ad, bd,
+                                         idesc_block_scaled<kKindNvf4>(128, 256, 0, 0), sfa, sfb,
+                                         (it | k) != 0);
       }
     }
     mma_commit(&bar);
@@ -416,7 +427,7 @@ int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, voi
 }
 
 int tg_probe_mma_rate(int kind, int iters, int ctas, unsigned long long* cycles, void* s) {
-  if (kind < 0 || kind > 2 || iters < 1 || iters > (1 << 20) || ctas < 1 || ctas > 4096 ||
+  if (kind < 0 || kind > 4 || iters < 1 || iters > (1 << 20) || ctas < 1 || ctas > 4096 ||
       cycles == nullptr)
     return TG_ERR_INVALID_ARG;
   DeviceCtx* ctx = current_ctx();
@@ -432,10 +443,18 @@ int tg_probe_mma_rate(int kind, int iters, int ctas, unsigned long long* cycles,
     e = cudaFuncSetAttribute(mma_rate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
       mma_rate_kernel<1><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
-  } else {
+  } else if (kind == 2) {
     e = cudaFuncSetAttribute(mma_rate_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
       mma_rate_kernel<2><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
+  } else if (kind == 3) {
+    e = cudaFuncSetAttribute(mma_rate_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      mma_rate_kernel<3><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
+  } else {
+    e = cudaFuncSetAttribute(mma_rate_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      mma_rate_kernel<4><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return launched();

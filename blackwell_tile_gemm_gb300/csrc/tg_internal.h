@@ -7,6 +7,7 @@
 
 #include "../../include/tgemm.h"
 #include "epilogue.cuh"
+#include "gemm_kinds.h"
 
 namespace tg {
 
@@ -38,8 +39,9 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
 // long (grown on demand).  nullptr on failure.
 void* device_workspace(size_t bytes);
 
-// Launchers (arguments already validated).
-int launch_gemm(bool mx, const void* A, int64_t lda, const void* B, int64_t ldb,
+// Launchers (arguments already validated).  kind: kKindBf16 or a
+// block-scaled kind (gemm_kinds.h).
+int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,
                 const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D,
                 int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype, const Epi& epi,
                 unsigned flags, cudaStream_t stream, DeviceCtx* ctx);
@@ -57,14 +59,29 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
                            const Epi& epi, bool pair, bool mcast, uint8_t* sf_workspace,
                            cudaStream_t stream, DeviceCtx* ctx);
 
-// Host-side argument checks of the block-scaled call (no CUDA calls).
-int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb, const void* SFA,
-                     int64_t ld_sfa, const void* SFB, int64_t ld_sfb, void* D, int64_t ldd,
-                     int64_t M, int64_t N, int64_t K, int d_dtype, int epilogue,
-                     unsigned flags);
+// Any block-scaled kind; sf_workspace holds blockscaled_workspace_bytes().
+int launch_gemm_blockscaled_impl(int kind, const void* A, int64_t lda, const void* B,
+                                 int64_t ldb, const void* SFA, int64_t ld_sfa, const void* SFB,
+                                 int64_t ld_sfb, void* D, int64_t ldd, int M, int N, int K,
+                                 int d_dtype, const Epi& epi, bool pair, bool mcast,
+                                 uint8_t* sf_workspace, cudaStream_t stream, DeviceCtx* ctx);
 
-// Bytes of scale-image workspace the MXFP8 path needs for this problem
-// (CTA pairs and multicast clusters share one image layout).
+// Host-side argument checks of a block-scaled call of `kind` (no CUDA calls).
+int check_blockscaled_args(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           int epilogue, unsigned flags);
+inline int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t ldb,
+                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                            void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                            int epilogue, unsigned flags) {
+  return check_blockscaled_args(kKindMxf8, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd, M,
+                                N, K, d_dtype, epilogue, flags);
+}
+
+// Bytes of scale-image workspace a block-scaled problem needs (CTA pairs and
+// multicast clusters share one image layout).
+size_t blockscaled_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K, bool pair);
 size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair);
 
 // D = epilogue(0) when K == 0.

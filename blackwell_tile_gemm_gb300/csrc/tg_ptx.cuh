@@ -12,6 +12,7 @@
 // hardware by the one-hot and exact-integer probe tests.
 #pragma once
 
+#include "gemm_kinds.h"
 #include <cstdint>
 #include <cuda.h>
 
@@ -389,6 +390,21 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t M, uint32_t N, u
          ((sfa_id & 3u) << 29);
 }
 
+// Instruction descriptor of a block-scaled kind: [4,6) B scale-factor id,
+// [7,10) / [10,13) A / B element format (E4M3 = 0 under .kind::mxf8f6f4,
+// E2M1 = 1 under .kind::mxf4nvf4), [17,23) N >> 3, [23] scale format
+// (1 = UE8M0, 0 = UE4M3), [24,29) M >> 4, [29,31) A scale-factor id.  Both
+// operands K-major.  The ids are the byte offsets inside the 32-bit scale
+// columns at which this MMA's scale vector starts.
+template <int kKind>
+__host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t M, uint32_t N, uint32_t sfa_id,
+                                                          uint32_t sfb_id) {
+  const uint32_t fmt = kKind == kKindMxf8 ? 0u : 1u;
+  const uint32_t ue8m0 = kKind == kKindNvf4 ? 0u : 1u;
+  return ((sfb_id & 3u) << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | (ue8m0 << 23) |
+         ((M >> 4) << 24) | ((sfa_id & 3u) << 29);
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: MMA, commit, copy, load
 // ---------------------------------------------------------------------------
@@ -439,6 +455,51 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
 }
 
 // Dense FP8: D (+)= A * B^T with E4M3 inputs, f32 accumulate (no scales).
+// Block-scaled MMA of kind kKind (see kKindMxf8 / kKindMxf4 / kKindNvf4):
+// D (+)= (A * SFA) * (B * SFB)^T with the scales read from TMEM.
+template <int kCtaGroup, int kKind>
+__device__ __forceinline__ void mma_block_scaled(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                 uint32_t accumulate) {
+  static_assert(kKind == kKindMxf8 || kKind == kKindMxf4 || kKind == kKindNvf4, "kind");
+  if constexpr (kKind == kKindMxf8) {
+    mma_mxf8<kCtaGroup>(d_tmem, a_desc, b_desc, idesc, sfa_tmem, sfb_tmem, accumulate);
+  } else if constexpr (kKind == kKindMxf4 && kCtaGroup == 1) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "setp.ne.b32 P, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X "
+        "[%0], %1, %2, %3, [%4], [%5], P;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  } else if constexpr (kKind == kKindMxf4) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "setp.ne.b32 P, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X "
+        "[%0], %1, %2, %3, [%4], [%5], P;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  } else if constexpr (kCtaGroup == 1) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "setp.ne.b32 P, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+        "[%0], %1, %2, %3, [%4], [%5], P;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "setp.ne.b32 P, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X "
+        "[%0], %1, %2, %3, [%4], [%5], P;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void mma_f8_dense(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(

@@ -65,13 +65,15 @@ enum { TG_D_F32 = 0, TG_D_BF16 = 1 };
  *   TG_EPI_SILU_AFFINE    D = silu(acc) * alpha + beta      (the pages' silu_affine)
  *   TG_EPI_BIAS_COL       D = acc + bias[j]
  *   TG_EPI_BIAS_COL_SILU  D = silu(acc + bias[j])
+ *   TG_EPI_AFFINE         D = acc * alpha + beta            (e.g. a per-tensor scale)
  * with silu(x) = x / (1 + exp(-x)) evaluated in f32 (CUDA expf). */
 enum {
   TG_EPI_NONE = 0,
   TG_EPI_ADD_SCALAR = 1,
   TG_EPI_SILU_AFFINE = 2,
   TG_EPI_BIAS_COL = 3,
-  TG_EPI_BIAS_COL_SILU = 4
+  TG_EPI_BIAS_COL_SILU = 4,
+  TG_EPI_AFFINE = 5
 };
 
 /* Epilogue description for the *_ex entry points (caller-owned, read during
@@ -155,6 +157,45 @@ int gemm_mxfp8_blockscaled_ex(const void* A, int64_t lda, const void* B, int64_t
                               void* D, int64_t ldd, int64_t M, int64_t N, int64_t K,
                               int d_dtype, const tg_epilogue* epi, unsigned flags,
                               void* cuda_stream);
+
+/*
+ * gemm_mxfp4_blockscaled -- block-scaled FP4 product with MX scales
+ * [MMA, .kind::mxf4nvf4 .block_scale .scale_vec::2X]:
+ *   D[i,j] = sum_k (a[i,k] * 2^(SFA[i,k/32]-127)) * (b[j,k] * 2^(SFB[j,k/32]-127))
+ *   A   : device, packed FP4 E2M1 [M, K/2] bytes, row stride lda (bytes):
+ *         element k of a row is the low nibble of byte k/2 for even k and
+ *         the high nibble for odd k.
+ *   B   : device, packed E2M1 [N, K/2] bytes, row stride ldb (bytes).
+ *   SFA : device, E8M0 bytes [M, K/32], row stride ld_sfa (>= K/32).
+ *   SFB : device, E8M0 bytes [N, K/32], row stride ld_sfb.
+ *   D, ldd, d_dtype, epi, flags: as for gemm_bf16_ex.
+ *   K must be a multiple of 32; otherwise TG_ERR_INVALID_ARG.  lda >= K/2,
+ *   ldb >= K/2, both multiples of 16 (TG_ERR_MISALIGNED).
+ * The scales are rearranged into the tensor-memory image in the same
+ * library-owned workspace as gemm_mxfp8_blockscaled (two 512-byte images per
+ * 128 rows and 256 K), with the same rule on concurrent calls.
+ */
+int gemm_mxfp4_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           const tg_epilogue* epi, unsigned flags, void* cuda_stream);
+
+/*
+ * gemm_nvfp4_blockscaled -- block-scaled FP4 product with UE4M3 scales per
+ * 16 elements [MMA, .kind::mxf4nvf4 .block_scale .scale_vec::4X]:
+ *   D[i,j] = sum_k (a[i,k] * ue4m3(SFA[i,k/16])) * (b[j,k] * ue4m3(SFB[j,k/16]))
+ *   A, B: packed E2M1 as for gemm_mxfp4_blockscaled.
+ *   SFA : device, UE4M3 bytes [M, K/16] (E4M3 with the sign bit clear; a set
+ *         sign bit or 0x7F is not a valid scale), row stride ld_sfa >= K/16.
+ *   SFB : device, UE4M3 bytes [N, K/16], row stride ld_sfb.
+ *   K must be a multiple of 16; otherwise TG_ERR_INVALID_ARG.  A per-tensor
+ *   scale (the second level of NVFP4 scaling) is applied with TG_EPI_AFFINE.
+ * Workspace: four 512-byte images per 128 rows and 256 K.
+ */
+int gemm_nvfp4_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
+                           const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
+                           void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,
+                           const tg_epilogue* epi, unsigned flags, void* cuda_stream);
 
 /*
  * gemm_mxfp8_blockscaled_noalloc -- the same product as gemm_mxfp8_blockscaled,

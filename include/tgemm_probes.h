@@ -60,7 +60,9 @@ int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, voi
  * ctas <= SM count), each issuing iters x 4 back-to-back M128 N256 MMAs on
  * fixed shared-memory operands into one TMEM accumulator.  kind: 0 = bf16
  * kind::f16 K16, 1 = E4M3 kind::mxf8f6f4.block_scale K32 (unit scales),
- * 2 = E4M3 kind::f8f6f4 K32.  cycles: device uint64 [2*ctas]; per CTA, SM
+ * 2 = E4M3 kind::f8f6f4 K32, 3 = packed E2M1 kind::mxf4nvf4.block_scale
+ * .scale_vec::2X K64 (unit E8M0 scales), 4 = the same with .scale_vec::4X
+ * (unit UE4M3 scales).  cycles: device uint64 [2*ctas]; per CTA, SM
  * clock cycles and then nanoseconds from the first issue to completion of
  * the last MMA.  Each CTA gets an SM of its own.  Dense
  * FLOP per SM per cycle = 2*128*256*K*4*iters / cycles.  This is the

@@ -103,7 +103,7 @@ def test_transpose_rejects_bad_arguments(L):
 
 
 @pytest.mark.parametrize("op,bias,code", [
-    (5, 0, tg.TG_ERR_INVALID_ARG),                  # unknown op
+    (6, 0, tg.TG_ERR_INVALID_ARG),                  # unknown op
     (-1, 0, tg.TG_ERR_INVALID_ARG),
     (tg.TG_EPI_BIAS_COL, 0, tg.TG_ERR_INVALID_ARG),  # bias op without a bias
     (tg.TG_EPI_BIAS_COL_SILU, A16 + 4, tg.TG_ERR_MISALIGNED),
@@ -124,3 +124,25 @@ def test_make_epilogue_rejects_two_ops():
         tg.make_epilogue(epilogue_add=1.0, silu_affine=(1.0, 0.0))
     e = tg.make_epilogue(silu_affine=(2.0, -1.0))
     assert (e.op, e.alpha, e.beta) == (tg.TG_EPI_SILU_AFFINE, 2.0, -1.0)
+
+
+@pytest.mark.parametrize("fn,block", [("gemm_mxfp4_blockscaled", 32),
+                                      ("gemm_nvfp4_blockscaled", 16)])
+def test_fp4_rejects_before_launch(L, fn, block):
+    f = getattr(L, fn)
+    ok = dict(A=A16, lda=64, B=A16, ldb=64, SFA=A16, ls=8, SFB=A16, lt=8, D=A16, ldd=64, M=64,
+              N=64, K=128, d=0, flags=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["A"], a["lda"], a["B"], a["ldb"], a["SFA"], a["ls"], a["SFB"], a["lt"],
+                 a["D"], a["ldd"], a["M"], a["N"], a["K"], a["d"], None, a["flags"], None)
+
+    assert call(K=block + block // 2) == tg.TG_ERR_INVALID_ARG          # K % block
+    assert call(lda=48, K=128) == tg.TG_ERR_INVALID_ARG                # lda < K/2 bytes
+    assert call(lda=72, K=128) == tg.TG_ERR_MISALIGNED                 # 72 % 16
+    assert call(ls=128 // block - 1) == tg.TG_ERR_INVALID_ARG          # ld_sfa < K/block
+    assert call(SFB=0) == tg.TG_ERR_INVALID_ARG
+    assert call(flags=3) == tg.TG_ERR_UNSUPPORTED                     # no FP4 multicast
+    assert call(M=0) == tg.TG_OK
