@@ -616,11 +616,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tmem_ld_wait();
       tc_fence_before_sync();
       __syncwarp();
+      // The reads are complete (wait::ld): a relaxed arrive hands the
+      // accumulator back without waiting for this warp's earlier D stores.
       if (lane == 0) {
         if constexpr (C::kCtaGroup == 1)
-          mbar_arrive(&acce_bar[acc]);
+          mbar_arrive_relaxed(&acce_bar[acc]);
         else
-          mbar_arrive_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+          mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
       }
       const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
       const int col_base = tn * C::BN + half * C::kEpiCols;
