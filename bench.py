@@ -53,13 +53,15 @@ _CSRC = "blackwell_tile_gemm_gb300/csrc/"
 KERNEL_SOURCES = {
     "gemm": [_CSRC + f for f in ("gemm_kernel.cuh", "tg_ptx.cuh", "gemm_launch.cuh",
                                  "gemm_kinds.h", "epilogue.cuh", "gemm_bf16.cu",
-                                 "gemm_blockscaled.cu")],
+                                 "gemm_blockscaled.cu", "gemm_fp4.cu")],
     "transpose": [_CSRC + f for f in ("transpose.cu", "tg_ptx.cuh")],
 }
 PROFILES = {
     "gemm_bf16": ("profiles/gemm_bf16_8192_pair.md", "gemm"),
     "gemm_mxfp8_blockscaled": ("profiles/gemm_mxfp8_8192_pair.md", "gemm"),
     "tile_transpose_b16": ("profiles/transpose_b16_8192.md", "transpose"),
+    "gemm_mxfp4_blockscaled": ("profiles/gemm_mxfp4_8192_pair.md", "gemm"),
+    "gemm_nvfp4_blockscaled": ("profiles/gemm_nvfp4_8192_pair.md", "gemm"),
 }
 
 
@@ -215,7 +217,15 @@ def run_ours(args, rank, world, local):
     run_bf16 = args.kernel in ("all", "gemm_bf16")
     run_mx = args.kernel in ("all", "gemm_mxfp8")
     run_tr = args.kernel in ("all", "transpose")
-    flops_step = flops_gemm * (int(run_bf16) + int(run_mx))
+    # FP4 GEMMs are not part of the step; --kernel times one of them alone.
+    run_f4 = args.kernel in ("gemm_mxfp4", "gemm_nvfp4")
+    if run_f4:
+        x4 = synth.make_inputs("mxf4_8k" if args.kernel == "gemm_mxfp4" else "nvf4_8k",
+                               M=SIZE, N=SIZE, K=SIZE)
+        f4 = {k: torch.from_numpy(x4[k]).to(dev) for k in ("A", "B", "SFA", "SFB")}
+        f4_call = tg.gemm_mxfp4_blockscaled if args.kernel == "gemm_mxfp4" \
+            else tg.gemm_nvfp4_blockscaled
+    flops_step = flops_gemm * (int(run_bf16) + int(run_mx) + int(run_f4))
 
     def step(ev=None):
         if ev is not None:
@@ -227,6 +237,8 @@ def run_ours(args, rank, world, local):
         if run_mx:
             tg.gemm_mxfp8_blockscaled(d["mA"], d["mB"], d["SFA"], d["SFB"], d["mD"],
                                       cta_pair=True, stream=stream)
+        if run_f4:
+            f4_call(f4["A"], f4["B"], f4["SFA"], f4["SFB"], d["mD"], cta_pair=True, stream=stream)
         if ev is not None:
             ev[2].record(stream)
         if run_tr:
@@ -277,6 +289,10 @@ def run_ours(args, rank, world, local):
         t = flops_gemm / (mx_ms * 1e-3) / 1e12
         kern["gemm_mxfp8_blockscaled"] = {"ms": mx_ms, "tflops": t,
                                           "frac_of_2x_bf16_peak": t / (2 * peak_bf16)}
+    if run_f4:
+        t = flops_gemm / (mx_ms * 1e-3) / 1e12
+        kern[f"{args.kernel}_blockscaled"] = {"ms": mx_ms, "tflops": t,
+                                              "frac_of_6x_bf16_peak": t / (6 * peak_bf16)}
     if run_tr:
         g = 2 * 2 * SIZE * SIZE / (tr_ms * 1e-3) / 1e9
         kern["tile_transpose_b16"] = {"ms": tr_ms, "gbs": g,
@@ -288,9 +304,12 @@ def run_ours(args, rank, world, local):
     elif dominant == "gemm_bf16":
         achieved, peak = kern["gemm_bf16"]["tflops"], peak_bf16
         peak_note = f"bf16 cuBLAS burst, {peak_src}"
-    else:
+    elif dominant == "gemm_mxfp8_blockscaled":
         achieved, peak = kern[dominant]["tflops"], 2 * peak_bf16
         peak_note = f"2 x bf16 cuBLAS burst (fp8/bf16 nominal ratio), {peak_src}"
+    else:
+        achieved, peak = kern[dominant]["tflops"], 6 * peak_bf16
+        peak_note = f"6 x bf16 cuBLAS burst (fp4/bf16 nominal ratio), {peak_src}"
     roofline = {"bound": "hbm" if dominant == "tile_transpose_b16" else "tensor",
                 "kernel": dominant, "achieved": achieved, "peak": peak,
                 "unit": "GB/s" if dominant == "tile_transpose_b16" else "TFLOP/s",
@@ -306,7 +325,8 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT if flops_step else "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3 (f32 accumulate)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1 (f32 accumulate)" if run_f4 else "bf16+e4m3 (f32 accumulate)",
         "data": "synthetic (seeded numpy; recipes in blackwell_tile_gemm_gb300/synth.py)",
         "config": {"workload": workload() if args.kernel == "all" else f"{args.kernel} only",
                    "M": SIZE, "N": SIZE, "K": SIZE,
@@ -314,7 +334,8 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "not flushed: 516 MB of step inputs > 129 MB L2"},
         "roofline": roofline, "kernels": kern, "e2e": e2e,
-        "gpu_launches": (int(run_bf16) + 2 * int(run_mx) + int(run_tr)) * args.steps,
+        "gpu_launches": (int(run_bf16) + 2 * int(run_mx) + 2 * int(run_f4) + int(run_tr))
+        * args.steps,
         "clocks": clk.summary(),
     }
     if cpu is not None:
@@ -614,7 +635,8 @@ def main(argv=None):
                     help="time every workload of the table (one JSON line each) and exit")
     ap.add_argument("--size", type=int, default=8192,
                     help="M = N = K of the GEMMs and the transpose side (default 8192)")
-    ap.add_argument("--kernel", choices=["all", "gemm_bf16", "gemm_mxfp8", "transpose"],
+    ap.add_argument("--kernel", choices=["all", "gemm_bf16", "gemm_mxfp8", "transpose",
+                                         "gemm_mxfp4", "gemm_nvfp4"],
                     default="all", help="run one part of the step only (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

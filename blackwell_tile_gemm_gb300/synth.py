@@ -109,12 +109,23 @@ _E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.f
 
 def f32_to_e2m1_codes(x: np.ndarray) -> np.ndarray:
     """Round to FP4 E2M1 (nearest, ties to the even code), saturating at +-6;
-    one 4-bit code per uint8 (sign in bit 3)."""
-    x = np.asarray(x, dtype=np.float64)
-    a = np.minimum(np.abs(x), 6.0)
-    # nearest magnitude; on an exact midpoint take the code with fraction bit 0
-    d = np.abs(a[..., None] - _E2M1_MAGNITUDES)
-    best = np.argmin(d + (np.arange(8) & 1) * 1e-12, axis=-1).astype(np.uint8)
+    one 4-bit code per uint8 (sign in bit 3).  NaN encodes as 0."""
+    x = np.asarray(x, dtype=np.float32)
+    # The code of |x| is the number of midpoints between neighbouring
+    # magnitudes that lie below |x|; on an exact midpoint (between codes c and
+    # c+1) the even code wins.  All midpoints are multiples of 1/4, so with
+    # q = 4|x| (exact) and j = floor(q) the count comes from small tables.
+    q = np.minimum(np.abs(x), np.float32(6.0)) * np.float32(4.0)
+    q = np.where(np.isnan(q), np.float32(0.0), q)     # E2M1 has no NaN: encode 0
+    j = q.astype(np.int32)
+    exact = q == j
+    mid_q = ((_E2M1_MAGNITUDES[:-1] + _E2M1_MAGNITUDES[1:]) * 2).astype(np.int32)
+    grid = np.arange(25)
+    cnt_le = (mid_q[None, :] <= grid[:, None]).sum(1).astype(np.uint8)
+    cnt_lt = (mid_q[None, :] < grid[:, None]).sum(1).astype(np.uint8)
+    is_mid = np.isin(grid, mid_q)
+    c = np.where(exact, cnt_lt[j], cnt_le[j])
+    best = (c + (exact & is_mid[j] & (c % 2 == 1))).astype(np.uint8)
     sign = (np.signbit(x) & (best != 0)).astype(np.uint8)
     return (sign << 3) | best
 
