@@ -442,18 +442,20 @@ def run_configs(args):
     dev = torch.device("cuda", 0)
     peaks, _ = measured_peaks()
     def median_ms(fn):
+        # median over 5 rounds of 10 back-to-back calls (per call), after warm-up
         for _ in range(5):
             fn()
         torch.cuda.synchronize()
         times = []
-        for _ in range(20):
+        for _ in range(5):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
-            fn()
+            for _ in range(10):
+                fn()
             e1.record()
             torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1))
+            times.append(e0.elapsed_time(e1) / 10)
         return statistics.median(times)
 
     # Fused-epilogue rows: the same 8192^3 products with each non-trivial op.
@@ -483,15 +485,29 @@ def run_configs(args):
                             dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
             if not epi and w.epi_add:
                 epi = dict(epilogue_add=w.epi_add)
-            fn = lambda: tg.gemm_bf16(A, B, D, cta_pair=w.cta_pair, **epi)  # noqa: E731
+            if w.kind == "skinny":
+                fn = lambda: tg.gemm_bf16_skinny(A, B, D, **epi)  # noqa: E731
+                # the same product through the 128 x 256 tile kernel, for comparison
+                ms_tile = median_ms(lambda: tg.gemm_bf16(A, B, D))
+            else:
+                fn = lambda: tg.gemm_bf16(A, B, D, cta_pair=w.cta_pair, **epi)  # noqa: E731
         ms = median_ms(fn)
         code, _ = tg.tg_device_status()
-        line = {"workload": name, "describe": w.describe, "status": code, "ms_median": ms}
+        line = {"workload": name, "describe": w.describe, "status": code, "ms_median": ms,
+                "timing": "median of 5 rounds of 10 back-to-back calls"}
         if epi:
             line["epilogue"] = sorted(epi)
         if w.kind == "transpose":
             gbs = 2 * 2 * w.M * w.N / (ms * 1e-3) / 1e9
             line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]))
+        elif w.kind == "skinny":
+            # algorithmic bytes: B and A read once, D written once (bf16)
+            nbytes = 2 * w.N * w.K + 2 * w.M * w.K + 2 * w.M * w.N
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]),
+                        tflops=w.flops / (ms * 1e-3) / 1e12,
+                        splits=tg.skinny_split_count(w.N, w.K, 0),
+                        tile_kernel_ms=ms_tile)
         else:
             tf = w.flops / (ms * 1e-3) / 1e12
             # nominal dense ratios to bf16 (2.25 / 4.5 / 13.5 PFLOP/s per GPU)

@@ -85,6 +85,11 @@ def lib() -> ctypes.CDLL:
         L.gemm_mxfp8_blockscaled_ex.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                                 i64, i64, i64, i32, ctypes.POINTER(tg_epilogue),
                                                 u32, vp]
+        L.gemm_bf16_skinny.restype = i32
+        L.gemm_bf16_skinny.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
+                                       ctypes.POINTER(tg_epilogue), i32, vp]
+        L.tg_skinny_split_count.restype = i32
+        L.tg_skinny_split_count.argtypes = [i64, i64, i32]
         for name in ("gemm_mxfp4_blockscaled", "gemm_nvfp4_blockscaled"):
             getattr(L, name).restype = i32
             getattr(L, name).argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64,
@@ -250,6 +255,43 @@ def gemm_mxfp8_blockscaled(A, B, SFA, SFB, D=None, *, out_dtype=None, epilogue_a
         _flags(cta_pair, multicast), _stream_handle(stream))
     _check(rc, "gemm_mxfp8_blockscaled")
     return D
+
+
+def gemm_bf16_skinny(A, B, D=None, *, out_dtype=None, epilogue_add=None, silu_affine=None,
+                     bias=None, bias_silu=False, affine=None, split_k=0, stream=None):
+    """D = A @ B.T (+ epilogue) for few rows of A (1 <= M <= 128).
+
+    Same operands as ``gemm_bf16``; the kernel is built for reading B once
+    from HBM (operands swapped, K split into ``split_k`` pieces reduced with
+    TMA reduce-add; 0 = automatic).  D float32 or bfloat16 (default float32).
+    """
+    import torch
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A is [M, K] and B is [N, K]")
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    if D is None:
+        D = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    if tuple(D.shape) != (M, N):
+        raise ValueError("D must be [M, N]")
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias must have N elements")
+    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu, affine)
+    rc = lib().gemm_bf16_skinny(A.data_ptr(), _ld(A, "A", 8), B.data_ptr(), _ld(B, "B", 8),
+                                D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype),
+                                ctypes.byref(epi), int(split_k), _stream_handle(stream))
+    _check(rc, "gemm_bf16_skinny")
+    return D
+
+
+def skinny_split_count(N: int, K: int, split_k: int = 0) -> int:
+    """K pieces gemm_bf16_skinny uses on the current device."""
+    r = lib().tg_skinny_split_count(int(N), int(K), int(split_k))
+    if r < 0:
+        raise TgError(-r, "tg_skinny_split_count")
+    return r
 
 
 def _gemm_fp4(fn_name, block, A, B, SFA, SFB, D, out_dtype, epi_kw, cta_pair, stream):

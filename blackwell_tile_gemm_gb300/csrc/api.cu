@@ -313,6 +313,38 @@ int gemm_fp4_common(int kind, const void* A, int64_t lda, const void* B, int64_t
 
 extern "C" {
 
+int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+                     int64_t M, int64_t N, int64_t K, int d_dtype, const tg_epilogue* epi,
+                     int split_k, void* cuda_stream) {
+  Epi e;
+  int rc = check_epilogue(epi, &e);
+  if (rc != TG_OK) return rc;
+  if (split_k < 0) return TG_ERR_INVALID_ARG;
+  rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, TG_EPI_NONE, 0, 2);
+  if (rc != TG_OK || M == 0 || N == 0) return rc;
+  if (M > 128) return TG_ERR_UNSUPPORTED;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  cudaStream_t stream = as_stream(cuda_stream);
+  if (K == 0) return launch_fill_epilogue(D, ldd, M, N, d_dtype, e, stream);
+  float* ws = nullptr;
+  const size_t ws_bytes = skinny_workspace_bytes(M, N, d_dtype, e.op);
+  if (ws_bytes) {
+    ws = static_cast<float*>(device_workspace(ws_bytes));
+    if (ws == nullptr) return TG_ERR_CUDA;
+  }
+  return launch_gemm_skinny_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M), static_cast<int>(N),
+                                 static_cast<int>(K), d_dtype, e, split_k, ws, stream, ctx);
+}
+
+int tg_skinny_split_count(int64_t N, int64_t K, int split_k) {
+  if (N < 1 || K < 1 || split_k < 0 || N > kMaxDim || K > kMaxDim) return -TG_ERR_INVALID_ARG;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return -TG_ERR_CUDA;
+  int per = 0;
+  return skinny_splits(N, K, split_k, ctx->num_sms, &per);
+}
+
 int gemm_mxfp4_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, int d_dtype,

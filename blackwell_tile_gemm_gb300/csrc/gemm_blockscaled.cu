@@ -45,6 +45,7 @@ struct SfImage {
   int rows;
   int blocks;           // 128-row blocks per stage in the image
   uint32_t* dst;        // [num_kg / groups][blocks][groups][128] words
+  int vec16;            // src and ld are 16-byte aligned: whole chunks load as uint4
 };
 
 // Scale group g (scales 4g .. 4g+3 of each row) belongs to stage g / groups
@@ -74,11 +75,19 @@ __global__ void sf_repack_kernel(SfImage a, SfImage b, int kblocks, int num_kg, 
     const int row = blk * 128 + 32 * j + l;
     uint32_t v[4] = {0, 0, 0, 0};
     if (row < s.rows) {
-      const uint8_t* src = s.src + static_cast<int64_t>(row) * s.ld;
+      const uint8_t* src = s.src + static_cast<int64_t>(row) * s.ld + 16 * quad;
+      if (16 * quad + 16 <= kblocks && s.vec16) {
+        // The 16 scales of this quad are a 16-byte aligned chunk of the row.
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(src));
+        v[0] = q.x;
+        v[1] = q.y;
+        v[2] = q.z;
+        v[3] = q.w;
+      } else {
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const int kb = 16 * quad + t;
-        if (kb < kblocks) v[t >> 2] |= static_cast<uint32_t>(__ldg(src + kb)) << (8 * (t & 3));
+        for (int t = 0; t < 16; ++t)
+          if (16 * quad + t < kblocks)
+            v[t >> 2] |= static_cast<uint32_t>(__ldg(src + t)) << (8 * (t & 3));
       }
     }
 #pragma unroll
@@ -137,10 +146,13 @@ int launch_gemm_blockscaled_impl(int kind, const void* A, int64_t lda, const voi
   uint8_t* img_a = sf_workspace;
   uint8_t* img_b = sf_workspace + static_cast<size_t>(pl.sfa_blocks) * pl.num_kg * 512u;
 
+  auto vec16 = [](const void* p, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(p) % 16 == 0 && ld % 16 == 0) ? 1 : 0;
+  };
   SfImage sa{static_cast<const uint8_t*>(SFA), ld_sfa, M, pl.sfa_blocks,
-             reinterpret_cast<uint32_t*>(img_a)};
+             reinterpret_cast<uint32_t*>(img_a), vec16(SFA, ld_sfa)};
   SfImage sb{static_cast<const uint8_t*>(SFB), ld_sfb, N, pl.sfb_blocks,
-             reinterpret_cast<uint32_t*>(img_b)};
+             reinterpret_cast<uint32_t*>(img_b), vec16(SFB, ld_sfb)};
   const int64_t warps =
       static_cast<int64_t>((pl.num_kg + 3) / 4) * (pl.sfa_blocks + pl.sfb_blocks) * 4;
   int64_t blocks = (warps + 7) / 8;

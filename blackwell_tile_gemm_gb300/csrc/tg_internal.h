@@ -84,6 +84,16 @@ inline int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t l
 size_t blockscaled_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K, bool pair);
 size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair);
 
+// Skinny bf16 GEMM (M <= 128): split-K pieces reduce into an f32 target.
+// `workspace` (f32, skinny_workspace_bytes) is used for bf16 D only.
+int launch_gemm_skinny_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
+                            int64_t ldd, int M, int N, int K, int d_dtype, const Epi& epi,
+                            int split_k, float* workspace, cudaStream_t stream, DeviceCtx* ctx);
+size_t skinny_workspace_bytes(int64_t M, int64_t N, int d_dtype, int epi_op);
+// K pieces per tile for split_k (0: automatic); *per_split = 64-element
+// stages per piece.
+int skinny_splits(int64_t N, int64_t K, int split_k, int num_sms, int* per_split);
+
 // D = epilogue(0) when K == 0.
 int launch_fill_epilogue(void* D, int64_t ldd, int64_t M, int64_t N, int d_dtype, const Epi& epi,
                          cudaStream_t stream);

@@ -169,7 +169,7 @@ def b16_bits(rng: np.random.Generator, shape) -> np.ndarray:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str          # "bf16", "mxfp8", "mxfp4", "nvfp4" or "transpose"
+    kind: str          # "bf16", "skinny", "mxfp8", "mxfp4", "nvfp4" or "transpose"
     M: int
     N: int
     K: int
@@ -197,6 +197,10 @@ WORKLOADS = {
                        "bf16 GEMM 4000x3000x1000 + 1, U[-1,1) inputs, fp32 D"),
     "tr8k": Workload("tr8k", "transpose", 8192, 8192, 0, 6, "b16", 0.0, False,
                      "b16 transpose 8192x8192, random bit patterns"),
+    "sk16_8k": Workload("sk16_8k", "skinny", 16, 8192, 8192, 9, "bf16", 0.0, False,
+                        "skinny bf16 GEMM 16x8192x8192 (B read once from HBM), bf16 D"),
+    "sk64_8k": Workload("sk64_8k", "skinny", 64, 8192, 8192, 10, "bf16", 0.0, False,
+                        "skinny bf16 GEMM 64x8192x8192, bf16 D"),
     "mxf4_8k": Workload("mxf4_8k", "mxfp4", 8192, 8192, 8192, 7, "bf16", 0.0, True,
                         "MXFP4 GEMM 8192^3, E2M1 x E8M0/32 inputs, bf16 D"),
     "nvf4_8k": Workload("nvf4_8k", "nvfp4", 8192, 8192, 8192, 8, "bf16", 0.0, True,
@@ -245,6 +249,8 @@ def make_inputs(w: Workload | str, M: int | None = None, N: int | None = None,
             "SFA": ue4m3_pow2_scales(rng, (M, K // 16)),
             "SFB": ue4m3_pow2_scales(rng, (N, K // 16)),
         }
+    if w.kind == "skinny":
+        return {"A": bf16_normal(rng, (M, K), 1.0 / math.sqrt(K)), "B": bf16_normal(rng, (N, K))}
     if w.name in ("tiny", "ragged"):
         return {"A": bf16_uniform(rng, (M, K)), "B": bf16_uniform(rng, (N, K))}
     if w.name == "sq8k":

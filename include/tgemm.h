@@ -159,6 +159,29 @@ int gemm_mxfp8_blockscaled_ex(const void* A, int64_t lda, const void* B, int64_t
                               void* cuda_stream);
 
 /*
+ * gemm_bf16_skinny -- gemm_bf16_ex for few rows (1 <= M <= 128), where reading
+ * B once from HBM bounds the product.  The operands are swapped so that 128
+ * rows of B fill the MMA's M side and the M rows of A its N side (rounded up
+ * to 16, 32, 64 or 128); every 128-row tile of B is split into split_k pieces
+ * of K (0: chosen from N, K and the SM count) whose f32 partial tiles are
+ * added into the result with TMA reduce-add ["cp.async.bulk.tensor",
+ * reductions].  D, ldd, d_dtype, epi: as for gemm_bf16_ex.
+ *   M > 128: TG_ERR_UNSUPPORTED; split_k < 0: TG_ERR_INVALID_ARG.
+ * With more than one piece the partial sums are added in a run-dependent
+ * order, so the last bits of D may differ between runs.  bf16 D, and f32 D
+ * with a SiLU epilogue, take one extra elementwise pass; bf16 D uses the
+ * library workspace (M * ceil(N/4)*4 * 4 bytes), with the same rule on
+ * concurrent calls as the block-scaled calls.
+ */
+int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+                     int64_t M, int64_t N, int64_t K, int d_dtype, const tg_epilogue* epi,
+                     int split_k, void* cuda_stream);
+
+/* tg_skinny_split_count -- the number of K pieces gemm_bf16_skinny uses for
+ * (N, K, split_k) on the current device, or minus a status code. */
+int tg_skinny_split_count(int64_t N, int64_t K, int split_k);
+
+/*
  * gemm_mxfp4_blockscaled -- block-scaled FP4 product with MX scales
  * [MMA, .kind::mxf4nvf4 .block_scale .scale_vec::2X]:
  *   D[i,j] = sum_k (a[i,k] * 2^(SFA[i,k/32]-127)) * (b[j,k] * 2^(SFB[j,k/32]-127))

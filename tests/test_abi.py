@@ -146,3 +146,13 @@ def test_fp4_rejects_before_launch(L, fn, block):
     assert call(SFB=0) == tg.TG_ERR_INVALID_ARG
     assert call(flags=3) == tg.TG_ERR_UNSUPPORTED                     # no FP4 multicast
     assert call(M=0) == tg.TG_OK
+
+
+def test_skinny_rejects_before_launch(L):
+    f = L.gemm_bf16_skinny
+    base = (A16, 64, A16, 64, A16, 64)
+    assert f(*base, 129, 64, 64, 0, None, 0, None) == tg.TG_ERR_UNSUPPORTED    # M > 128
+    assert f(*base, 16, 64, 64, 0, None, -1, None) == tg.TG_ERR_INVALID_ARG    # split_k < 0
+    assert f(*base, 16, 64, 64, 7, None, 0, None) == tg.TG_ERR_INVALID_ARG     # d_dtype
+    assert f(A16 + 2, 64, A16, 64, A16, 64, 16, 64, 64, 0, None, 0, None) == tg.TG_ERR_MISALIGNED
+    assert f(*base, 0, 64, 64, 0, None, 0, None) == tg.TG_OK
