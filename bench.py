@@ -465,6 +465,8 @@ def run_configs(args):
     rows = [(name, w, {}) for name, w in synth.WORKLOADS.items()]
     rows += [(f"{base}+{op}", synth.WORKLOADS[base], kw) for base in ("sq8k", "mx8k")
              for op, kw in epilogue_rows.items()]
+    # the gathered-row product with the rows loaded inside the GEMM by gather4
+    rows += [("moe_8k+gather_tma", synth.WORKLOADS["moe_8k"], {"gather_tma": True})]
     for name, w, epi in rows:
         x = synth.make_inputs(w)
         if w.kind == "transpose":
@@ -485,7 +487,12 @@ def run_configs(args):
                             dtype=torch.bfloat16 if w.d_dtype == "bf16" else torch.float32)
             if not epi and w.epi_add:
                 epi = dict(epilogue_add=w.epi_add)
-            if w.kind == "skinny":
+            if w.kind == "gather":
+                idx = torch.from_numpy(x["idx"]).to(dev)
+                fn = lambda: tg.gemm_bf16_gather(A, idx, B, D, cta_pair=w.cta_pair, **epi)  # noqa
+                # the dense product of the same shape (A rows in place), for comparison
+                ms_tile = median_ms(lambda: tg.gemm_bf16(A[:w.M], B, D, cta_pair=w.cta_pair))
+            elif w.kind == "skinny":
                 fn = lambda: tg.gemm_bf16_skinny(A, B, D, **epi)  # noqa: E731
                 # the same product through the 128 x 256 tile kernel, for comparison
                 ms_tile = median_ms(lambda: tg.gemm_bf16(A, B, D))
@@ -508,6 +515,10 @@ def run_configs(args):
                         tflops=w.flops / (ms * 1e-3) / 1e12,
                         splits=tg.skinny_split_count(w.N, w.K, 0),
                         tile_kernel_ms=ms_tile)
+        elif w.kind == "gather":
+            tf = w.flops / (ms * 1e-3) / 1e12
+            line.update(tflops=tf, frac_of_cublas_bf16_burst_scaled=tf / float(peaks["bf16_tflops"]),
+                        dense_same_shape_ms=ms_tile)
         else:
             tf = w.flops / (ms * 1e-3) / 1e12
             # nominal dense ratios to bf16 (2.25 / 4.5 / 13.5 PFLOP/s per GPU)

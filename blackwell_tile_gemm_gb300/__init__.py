@@ -39,6 +39,7 @@ TG_EPI_BIAS_COL_SILU = 4
 TG_EPI_AFFINE = 5
 TG_FLAG_CTA_PAIR = 1
 TG_FLAG_MULTICAST = 2
+TG_FLAG_GATHER_TMA = 4
 
 _lock = threading.Lock()
 _lib = None
@@ -88,6 +89,9 @@ def lib() -> ctypes.CDLL:
         L.gemm_bf16_skinny.restype = i32
         L.gemm_bf16_skinny.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
                                        ctypes.POINTER(tg_epilogue), i32, vp]
+        L.gemm_bf16_gather.restype = i32
+        L.gemm_bf16_gather.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp, i64, i64, i64, i32,
+                                       ctypes.POINTER(tg_epilogue), u32, vp]
         L.tg_skinny_split_count.restype = i32
         L.tg_skinny_split_count.argtypes = [i64, i64, i32]
         for name in ("gemm_mxfp4_blockscaled", "gemm_nvfp4_blockscaled"):
@@ -283,6 +287,40 @@ def gemm_bf16_skinny(A, B, D=None, *, out_dtype=None, epilogue_add=None, silu_af
                                 D.data_ptr(), _ld(D, "D", 8), M, N, K, _d_code(D.dtype),
                                 ctypes.byref(epi), int(split_k), _stream_handle(stream))
     _check(rc, "gemm_bf16_skinny")
+    return D
+
+
+def gemm_bf16_gather(A, row_idx, B, D=None, *, out_dtype=None, epilogue_add=None,
+                     silu_affine=None, bias=None, bias_silu=False, affine=None, cta_pair=False,
+                     gather_tma=False, stream=None):
+    """D[i] = A[row_idx[i]] @ B.T (+ epilogue): rows of A gathered by index.
+
+    A: bfloat16 [a_rows, K]; row_idx: int32 CUDA vector [M] (indices outside
+    [0, a_rows) give zero rows); B: bfloat16 [N, K].  D float32 or bfloat16
+    [M, N] (default float32).  ``gather_tma`` loads the rows inside the GEMM
+    with TMA gather4 instead of gathering them into the workspace first.
+    """
+    import torch
+    a_rows, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A is [a_rows, K] and B is [N, K]")
+    if row_idx.dtype != torch.int32 or row_idx.dim() != 1 or not row_idx.is_contiguous():
+        raise TypeError("row_idx must be a contiguous int32 vector")
+    M = row_idx.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    if tuple(D.shape) != (M, N):
+        raise ValueError("D must be [M, N]")
+    if bias is not None and bias.shape[0] != N:
+        raise ValueError("bias must have N elements")
+    epi = make_epilogue(epilogue_add, silu_affine, bias, bias_silu, affine)
+    rc = lib().gemm_bf16_gather(A.data_ptr(), _ld(A, "A", 8), a_rows, row_idx.data_ptr(), M,
+                                B.data_ptr(), _ld(B, "B", 8), D.data_ptr(), _ld(D, "D", 8), N, K,
+                                _d_code(D.dtype), ctypes.byref(epi),
+                                _flags(cta_pair, False) | (TG_FLAG_GATHER_TMA if gather_tma else 0),
+                                _stream_handle(stream))
+    _check(rc, "gemm_bf16_gather")
     return D
 
 

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtgemm.so")
 SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_blockscaled.cu", "gemm_fp4.cu", "gemm_skinny.cu",
-           "gemm_mxfp8_noalloc.cu", "transpose.cu", "probes.cu"]
+           "gemm_gather.cu", "gemm_mxfp8_noalloc.cu", "transpose.cu", "probes.cu"]
 HEADERS = ["tg_ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh", "tg_internal.h", "epilogue.cuh",
            "gemm_kinds.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -337,6 +337,38 @@ int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, voi
                                  static_cast<int>(K), d_dtype, e, split_k, ws, stream, ctx);
 }
 
+int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* row_idx,
+                     int64_t M, const void* B, int64_t ldb, void* D, int64_t ldd, int64_t N,
+                     int64_t K, int d_dtype, const tg_epilogue* epi, unsigned flags,
+                     void* cuda_stream) {
+  Epi e;
+  int rc = check_epilogue(epi, &e);
+  if (rc != TG_OK) return rc;
+  if (flags & TG_FLAG_MULTICAST) return TG_ERR_UNSUPPORTED;
+  if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR | TG_FLAG_GATHER_TMA))
+    return TG_ERR_UNSUPPORTED;
+  if (a_rows < 0 || a_rows > kMaxDim) return TG_ERR_INVALID_ARG;
+  // A is checked as an [a_rows, K] operand, D as [M, N].
+  rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, TG_EPI_NONE,
+                         flags & TG_FLAG_CTA_PAIR, 2);
+  if (rc != TG_OK || M == 0 || N == 0) return rc;
+  if (K > 0 && (row_idx == nullptr || a_rows == 0)) return TG_ERR_INVALID_ARG;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  cudaStream_t stream = as_stream(cuda_stream);
+  if (K == 0) return launch_fill_epilogue(D, ldd, M, N, d_dtype, e, stream);
+  const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
+  if (flags & TG_FLAG_GATHER_TMA)
+    return launch_gemm_bf16_gather_impl(A, lda, static_cast<int>(a_rows), row_idx,
+                                        static_cast<int>(M), B, ldb, D, ldd, static_cast<int>(N),
+                                        static_cast<int>(K), d_dtype, e, pair, stream, ctx);
+  void* ws = device_workspace(gather_workspace_bytes(M, K));
+  if (ws == nullptr) return TG_ERR_CUDA;
+  return launch_gemm_bf16_pregather_impl(A, lda, static_cast<int>(a_rows), row_idx,
+                                         static_cast<int>(M), B, ldb, D, ldd, static_cast<int>(N),
+                                         static_cast<int>(K), d_dtype, e, pair, ws, stream, ctx);
+}
+
 int tg_skinny_split_count(int64_t N, int64_t K, int split_k) {
   if (N < 1 || K < 1 || split_k < 0 || N > kMaxDim || K > kMaxDim) return -TG_ERR_INVALID_ARG;
   DeviceCtx* ctx = current_ctx();

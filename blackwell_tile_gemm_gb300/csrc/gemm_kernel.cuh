@@ -59,6 +59,8 @@ struct GemmArgs {
   int sfa_blocks;   // 128-row blocks per K group in the SFA image
   int sfb_blocks;   // 128-row blocks per K group in the SFB image
   int raster_group; // m-tiles per band of the tile order
+  const int* gather_idx;  // gathered A: D row i uses A row gather_idx[i] (else null)
+  int gather_rows;        // rows of A; indices outside [0, gather_rows) read zeros
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -66,8 +68,11 @@ struct GemmArgs {
 // kKind_: kKindBf16 (dense bf16) or one of the block-scaled kinds kKindMxf8,
 // kKindMxf4, kKindNvf4 (tg_ptx.cuh).
 template <int kCtaGroup_, int kKind_, int kBN_, int kAccBufs_, int kStages_, bool kBf16Out_,
-          bool kMcast_ = false>
+          bool kMcast_ = false, bool kGather_ = false>
 struct GemmCfg {
+  // Gathered A: the producer warp loads the A tile row by row with
+  // tile::gather4 (32 lanes x 4 rows = 128 rows), from GemmArgs::gather_idx.
+  static constexpr bool kGather = kGather_;
   static constexpr int kCtaGroup = kCtaGroup_;
   // Multicast: clusters of two CTA pairs that work on vertically adjacent
   // tiles share the B tile; each CTA loads a quarter of it and multicasts
@@ -135,13 +140,19 @@ struct GemmCfg {
   static constexpr int kEpiCols = BN / 2;
   static constexpr int kEpiChunks = kEpiCols / 32;
   static constexpr int kSfWarp0 = 2 + kEpiWarps;    // first scale-copy warp
-  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kSfWarps;
+  // Gathered A: warps 0 and kGatherWarp0.. issue the tile's 32 gather4 loads
+  // per stage together (a gather4 occupies its issuing thread for tens of
+  // cycles, so one warp cannot keep up with the MMAs).
+  static constexpr int kGatherWarps = kGather ? 3 : 1;
+  static constexpr int kGatherWarp0 = kSfWarp0 + kSfWarps;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kSfWarps + 32 * (kGatherWarps - 1);
   static_assert(TMEM_USED <= 512, "tensor memory has 512 columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(!kMcast || kCtaGroup == 2, "multicast clusters are made of CTA pairs");
   static_assert(!kMx || BN % 128 == 0, "scale images cover 128-row blocks of B");
+  static_assert(!kGather || (!kMx && !kMcast), "gathered A: bf16, without multicast");
 };
 
 // Grouped tile order: consecutive tile ids walk down a band of `group`
@@ -371,7 +382,90 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   // when a barrier is not ready, shared-memory descriptors are advanced by
   // adding offsets, and the next stage's barrier is probed while the current
   // stage's MMAs are queued.
-  if (warp == 0) {
+  if (C::kGather && (warp == 0 || (warp >= C::kGatherWarp0 &&
+                                    warp < C::kGatherWarp0 + C::kGatherWarps - 1))) {
+    // ------------------------------------------------ producer, gathered A
+    // kGatherWarps warps (gw = 0 .. kGatherWarps-1): each waits for a free
+    // slot itself; warp 0 posts the expected bytes and loads the B tile.
+    // Gather op j (rows 4j .. 4j+3 of the A tile, j < 32) belongs to warp
+    // j % kGatherWarps, lane j / kGatherWarps, which keeps the op's four row
+    // indices in registers for the tile.
+    if constexpr (C::kGather) {
+      const int gw = warp == 0 ? 0 : warp - C::kGatherWarp0 + 1;
+      const int op = gw + C::kGatherWarps * static_cast<int>(lane);
+      const bool has_op = op < 32;
+      const uint64_t pol_ab = policy_evict_last();
+      const uint32_t sA = smem_addr(smem + C::OFF_A);
+      const uint32_t sB = smem_addr(smem + C::OFF_B);
+      const uint32_t empty0 = smem_addr(&empty_bar[0]);
+      const uint32_t full0 = smem_addr(&full_bar[0]);
+      const uint32_t full_dst0 = C::kCtaGroup == 2 ? map_to_cta(full0, lead_rank) : full0;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;
+      bool ok = true;
+      for (int t = unit; t < num_tiles && ok; t += num_units) {
+        int tmc, tn;
+        tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
+        const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
+        const int a_row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM;
+        const int b_row = tn * C::BN + static_cast<int>(pair_rank) * C::B_ROWS;
+        int r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = a_row + 4 * op + j;
+          int src = has_op && i < p.M ? p.gather_idx[i] : p.gather_rows;
+          // Any index outside A is sent past its end, where the load reads zeros.
+          if (src < 0 || src >= p.gather_rows) src = p.gather_rows;
+          r[j] = src;
+        }
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          int got = 1;
+          if (lane == 0)
+            got = (mbar_try_wait(empty0 + 8u * stage, phase ^ 1u) ||
+                   mbar_wait(&empty_bar[stage], phase ^ 1u, guard, kSiteProducerEmpty))
+                      ? 1
+                      : 0;
+          got = __shfl_sync(0xFFFFFFFFu, got, 0);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          const int kx = kb * C::BK;
+          const uint32_t fb = full_dst0 + 8u * stage;
+          if (gw == 0 && lane == 0) {
+            if constexpr (C::kCtaGroup == 1) {
+              mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_TX);
+            } else {
+              if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_TX);
+            }
+          }
+          __syncwarp();
+          const uint32_t dstA = sA + stage * C::A_BYTES + static_cast<uint32_t>(op) * 512u;
+          if constexpr (C::kCtaGroup == 1) {
+            if (has_op) tma_gather4_2d(dstA, &tmA, fb, kx, r[0], r[1], r[2], r[3], pol_ab);
+            if (gw == 0 && lane == 0)
+              tma_load_2d(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+          } else {
+            if (has_op) tma_gather4_2d_pair(dstA, &tmA, fb, kx, r[0], r[1], r[2], r[3], pol_ab);
+            if (gw == 0 && lane == 0)
+              tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader && lane == 0) {
+        for (int s = 0; s < C::kStages; ++s)
+          if (issued & (1u << s))
+            mbar_wait_drain(&full_bar[s], (issued_parity >> s) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_ab = policy_evict_last();

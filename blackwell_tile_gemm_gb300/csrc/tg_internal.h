@@ -84,6 +84,20 @@ inline int check_mxfp8_args(const void* A, int64_t lda, const void* B, int64_t l
 size_t blockscaled_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K, bool pair);
 size_t mxfp8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool pair);
 
+// bf16 GEMM with A rows gathered by row_idx (device int32 [M]).
+int launch_gemm_bf16_gather_impl(const void* A, int64_t lda, int a_rows, const int* row_idx,
+                                 int M, const void* B, int64_t ldb, void* D, int64_t ldd, int N,
+                                 int K, int d_dtype, const Epi& epi, bool pair,
+                                 cudaStream_t stream, DeviceCtx* ctx);
+
+// Same product through a gathered copy of the rows in `workspace`
+// (gather_workspace_bytes) and the dense kernel.
+int launch_gemm_bf16_pregather_impl(const void* A, int64_t lda, int a_rows, const int* row_idx,
+                                    int M, const void* B, int64_t ldb, void* D, int64_t ldd,
+                                    int N, int K, int d_dtype, const Epi& epi, bool pair,
+                                    void* workspace, cudaStream_t stream, DeviceCtx* ctx);
+size_t gather_workspace_bytes(int64_t M, int64_t K);
+
 // Skinny bf16 GEMM (M <= 128): split-K pieces reduce into an f32 target.
 // `workspace` (f32, skinny_workspace_bytes) is used for bf16 D only.
 int launch_gemm_skinny_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,

@@ -258,6 +258,34 @@ __device__ __forceinline__ void tma_load_2d_pair_mcast(uint32_t dst, const CUten
       : "memory");
 }
 
+// Row gather ("cp.async.bulk.tensor", section "Gather4 and scatter4"): four
+// rows r0..r3 of a 2-D map whose box is one row high, columns x .. x+width,
+// into four consecutive box images at dst, completing on `bar`.  Rows
+// outside the tensor read as the fill value (zero).
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int32_t x, int32_t r0, int32_t r1, int32_t r2,
+                                               int32_t r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "l"(policy)
+      : "memory");
+}
+
+// Same, for a CTA pair: `bar` is a shared::cluster address (the leader's).
+__device__ __forceinline__ void tma_gather4_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                    uint32_t bar, int32_t x, int32_t r0,
+                                                    int32_t r1, int32_t r2, int32_t r3,
+                                                    uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled store shared -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y) {

@@ -169,7 +169,7 @@ def b16_bits(rng: np.random.Generator, shape) -> np.ndarray:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str          # "bf16", "skinny", "mxfp8", "mxfp4", "nvfp4" or "transpose"
+    kind: str          # "bf16", "skinny", "gather", "mxfp8", "mxfp4", "nvfp4", "transpose"
     M: int
     N: int
     K: int
@@ -201,6 +201,9 @@ WORKLOADS = {
                         "skinny bf16 GEMM 16x8192x8192 (B read once from HBM), bf16 D"),
     "sk64_8k": Workload("sk64_8k", "skinny", 64, 8192, 8192, 10, "bf16", 0.0, False,
                         "skinny bf16 GEMM 64x8192x8192, bf16 D"),
+    "moe_8k": Workload("moe_8k", "gather", 4096, 8192, 8192, 11, "bf16", 0.0, True,
+                       "gathered-row bf16 GEMM: 4096 of 16384 rows of A (sorted random) x "
+                       "8192x8192 B, bf16 D, CTA pairs"),
     "mxf4_8k": Workload("mxf4_8k", "mxfp4", 8192, 8192, 8192, 7, "bf16", 0.0, True,
                         "MXFP4 GEMM 8192^3, E2M1 x E8M0/32 inputs, bf16 D"),
     "nvf4_8k": Workload("nvf4_8k", "nvfp4", 8192, 8192, 8192, 8, "bf16", 0.0, True,
@@ -218,6 +221,7 @@ def make_inputs(w: Workload | str, M: int | None = None, N: int | None = None,
     mxfp4:     {"A": uint8 [M,K/2] packed E2M1, "B": uint8 [N,K/2],
                 "SFA": uint8 [M,K/32] E8M0, "SFB": uint8 [N,K/32]}
     nvfp4:     as mxfp4 with "SFA": uint8 [M,K/16] UE4M3, "SFB": uint8 [N,K/16]
+    gather:    {"A": uint16 [4M,K], "B": uint16 [N,K], "idx": int32 [M] rows of A}
     transpose: {"X": uint16 [M,N]}
     """
     if isinstance(w, str):
@@ -249,6 +253,12 @@ def make_inputs(w: Workload | str, M: int | None = None, N: int | None = None,
             "SFA": ue4m3_pow2_scales(rng, (M, K // 16)),
             "SFB": ue4m3_pow2_scales(rng, (N, K // 16)),
         }
+    if w.kind == "gather":
+        # M rows gathered from an A of 4M rows (a sorted random subset, the
+        # order in which a router's token list usually arrives)
+        return {"A": bf16_normal(rng, (4 * M, K), 1.0 / math.sqrt(K)),
+                "B": bf16_normal(rng, (N, K)),
+                "idx": np.sort(rng.choice(4 * M, M, replace=False)).astype(np.int32)}
     if w.kind == "skinny":
         return {"A": bf16_normal(rng, (M, K), 1.0 / math.sqrt(K)), "B": bf16_normal(rng, (N, K))}
     if w.name in ("tiny", "ragged"):

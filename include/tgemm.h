@@ -90,11 +90,15 @@ typedef struct tg_epilogue {
 enum {
   TG_FLAG_CTA_PAIR = 1u, /* cta_group::2: two CTAs of a cluster share one
                             256-row MMA; each loads half of the B tile      */
-  TG_FLAG_MULTICAST = 2u /* with TG_FLAG_CTA_PAIR only: clusters of two pairs
+  TG_FLAG_MULTICAST = 2u, /* with TG_FLAG_CTA_PAIR only: clusters of two pairs
                             on vertically adjacent tiles share the B tile by
                             TMA multicast (each CTA loads a quarter).  Same
                             results; on GB300 measured 2-3% slower than plain
                             pairs at 8192^3, so it is off by default.       */
+  TG_FLAG_GATHER_TMA = 4u /* gemm_bf16_gather only: load the gathered A rows
+                            inside the GEMM with TMA tile::gather4 instead
+                            of copying them into the workspace first.  Same
+                            results; slower on large shapes (see there).   */
 };
 
 /*
@@ -176,6 +180,29 @@ int gemm_mxfp8_blockscaled_ex(const void* A, int64_t lda, const void* B, int64_t
 int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
                      int64_t M, int64_t N, int64_t K, int d_dtype, const tg_epilogue* epi,
                      int split_k, void* cuda_stream);
+
+/*
+ * gemm_bf16_gather -- bf16 GEMM over gathered rows of A (a mixture-of-experts
+ * layer's tokens for one expert): D[i, :] = A[row_idx[i], :] * B^T (+ epi)
+ * for 0 <= i < M [MMA; TMA tile::gather4 loads of the A tile].
+ *   A       : device, bf16 [a_rows, K], row stride lda (elements).
+ *   row_idx : device, int32 [M]; any row of A, in any order, repeats allowed.
+ *             An index outside [0, a_rows) gives a zero row (D = epi(0)).
+ *   B, ldb, D, ldd, N, K, d_dtype, epi: as for gemm_bf16_ex; D is [M, N].
+ *   flags   : TG_FLAG_CTA_PAIR and / or TG_FLAG_GATHER_TMA (TG_FLAG_MULTICAST:
+ *             TG_ERR_UNSUPPORTED).
+ *   K > 0 with a NULL row_idx or a_rows == 0: TG_ERR_INVALID_ARG.
+ * By default the rows are first gathered into the library workspace
+ * (M * ceil(K/8)*8 * 2 bytes; same rule on concurrent calls as the
+ * block-scaled calls) and the dense kernel runs on them.  With
+ * TG_FLAG_GATHER_TMA the GEMM loads them itself with tile::gather4 (no
+ * workspace); that issue rate bounds it at ~60% of the dense kernel for
+ * 4096 x 8192 x 8192.
+ */
+int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* row_idx,
+                     int64_t M, const void* B, int64_t ldb, void* D, int64_t ldd, int64_t N,
+                     int64_t K, int d_dtype, const tg_epilogue* epi, unsigned flags,
+                     void* cuda_stream);
 
 /* tg_skinny_split_count -- the number of K pieces gemm_bf16_skinny uses for
  * (N, K, split_k) on the current device, or minus a status code. */

@@ -156,3 +156,21 @@ def test_skinny_rejects_before_launch(L):
     assert f(*base, 16, 64, 64, 7, None, 0, None) == tg.TG_ERR_INVALID_ARG     # d_dtype
     assert f(A16 + 2, 64, A16, 64, A16, 64, 16, 64, 64, 0, None, 0, None) == tg.TG_ERR_MISALIGNED
     assert f(*base, 0, 64, 64, 0, None, 0, None) == tg.TG_OK
+
+
+def test_gather_rejects_before_launch(L):
+    f = L.gemm_bf16_gather
+    assert f(A16, 64, 100, A16, 64, A16, 64, A16, 64, 64, 64, 0, None, 2, None) \
+        == tg.TG_ERR_UNSUPPORTED                                 # multicast
+    assert f(A16, 64, 100, 0, 64, A16, 64, A16, 64, 64, 64, 0, None, 0, None) \
+        == tg.TG_ERR_INVALID_ARG                                 # no row_idx
+    assert f(A16, 64, 0, A16, 64, A16, 64, A16, 64, 64, 64, 0, None, 0, None) \
+        == tg.TG_ERR_INVALID_ARG                                 # a_rows == 0
+    assert f(A16, 64, -1, A16, 64, A16, 64, A16, 64, 64, 64, 0, None, 0, None) \
+        == tg.TG_ERR_INVALID_ARG
+    assert f(A16, 64, 100, A16, 0, A16, 64, A16, 64, 64, 64, 0, None, 0, None) == tg.TG_OK
+    assert f(A16, 64, 100, A16, 64, A16, 64, A16, 64, 64, 64, 0, None, 8, None) \
+        == tg.TG_ERR_UNSUPPORTED                                 # unknown flag
+    # TG_FLAG_GATHER_TMA belongs to the gather call only
+    assert L.gemm_bf16(A16, 64, A16, 64, A16, 64, 64, 64, 64, 0, 0, 0.0, 4, None) \
+        == tg.TG_ERR_UNSUPPORTED
