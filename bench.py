@@ -467,6 +467,9 @@ def run_configs(args):
              for op, kw in epilogue_rows.items()]
     # the gathered-row product with the rows loaded inside the GEMM by gather4
     rows += [("moe_8k+gather_tma", synth.WORKLOADS["moe_8k"], {"gather_tma": True})]
+    if args.only:
+        keep = set(args.only.split(","))
+        rows = [r for r in rows if r[0] in keep]
     for name, w, epi in rows:
         x = synth.make_inputs(w)
         if w.kind == "transpose":
@@ -491,7 +494,8 @@ def run_configs(args):
                 idx = torch.from_numpy(x["idx"]).to(dev)
                 fn = lambda: tg.gemm_bf16_gather(A, idx, B, D, cta_pair=w.cta_pair, **epi)  # noqa
                 # the dense product of the same shape (A rows in place), for comparison
-                ms_tile = median_ms(lambda: tg.gemm_bf16(A[:w.M], B, D, cta_pair=w.cta_pair))
+                ms_tile = None if epi else median_ms(
+                    lambda: tg.gemm_bf16(A[:w.M], B, D, cta_pair=w.cta_pair))
             elif w.kind == "skinny":
                 fn = lambda: tg.gemm_bf16_skinny(A, B, D, **epi)  # noqa: E731
                 # the same product through the 128 x 256 tile kernel, for comparison
@@ -662,6 +666,8 @@ def main(argv=None):
                     help="time every workload of the table (one JSON line each) and exit")
     ap.add_argument("--size", type=int, default=8192,
                     help="M = N = K of the GEMMs and the transpose side (default 8192)")
+    ap.add_argument("--only", default="",
+                    help="with --configs: comma-separated workload rows to run (default all)")
     ap.add_argument("--kernel", choices=["all", "gemm_bf16", "gemm_mxfp8", "transpose",
                                          "gemm_mxfp4", "gemm_nvfp4"],
                     default="all", help="run one part of the step only (profiling)")
