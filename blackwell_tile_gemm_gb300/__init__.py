@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_bf16_gather.restype = i32
         L.gemm_bf16_gather.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp, i64, i64, i64, i32,
                                        ctypes.POINTER(tg_epilogue), u32, vp]
+        L.tg_gemm_tail_split.restype = i32
+        L.tg_gemm_tail_split.argtypes = [i64, i64, i64, u32]
         L.tg_skinny_split_count.restype = i32
         L.tg_skinny_split_count.argtypes = [i64, i64, i32]
         for name in ("gemm_mxfp4_blockscaled", "gemm_nvfp4_blockscaled"):
@@ -322,6 +324,14 @@ def gemm_bf16_gather(A, row_idx, B, D=None, *, out_dtype=None, epilogue_add=None
                                 _stream_handle(stream))
     _check(rc, "gemm_bf16_gather")
     return D
+
+
+def gemm_tail_split(M: int, N: int, K: int, cta_pair: bool = False) -> int:
+    """K pieces per tile of a last, partial wave that gemm_bf16 uses (1: none)."""
+    r = lib().tg_gemm_tail_split(int(M), int(N), int(K), TG_FLAG_CTA_PAIR if cta_pair else 0)
+    if r < 0:
+        raise TgError(-r, "tg_gemm_tail_split")
+    return r
 
 
 def skinny_split_count(N: int, K: int, split_k: int = 0) -> int:

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include <cuda.h>
@@ -114,6 +115,48 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
   return TG_OK;
+}
+
+namespace {
+struct TailScratch {
+  float* partials = nullptr;
+  uint32_t* flags = nullptr;
+};
+std::map<std::pair<int, uintptr_t>, TailScratch> g_tail;
+}  // namespace
+
+bool tail_scratch(cudaStream_t stream, float** partials, uint32_t** flags) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+  auto it = g_tail.find(key);
+  if (it == g_tail.end()) {
+    TailScratch t;
+    if (cudaMalloc(&t.partials, kTailPartialBytes) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (cudaMalloc(&t.flags, kTailFlagWords * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(t.flags, 0, kTailFlagWords * sizeof(uint32_t)) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(t.partials);
+      if (t.flags) cudaFree(t.flags);
+      return false;
+    }
+    it = g_tail.emplace(key, t).first;
+  }
+  *partials = it->second.partials;
+  *flags = it->second.flags;
+  return true;
+}
+
+void reset_tail_flags() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  for (auto& kv : g_tail)
+    if (kv.first.first == dev) cudaMemset(kv.second.flags, 0, kTailFlagWords * sizeof(uint32_t));
 }
 
 void* device_workspace(size_t bytes) {
@@ -369,6 +412,15 @@ int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* 
                                          static_cast<int>(K), d_dtype, e, pair, ws, stream, ctx);
 }
 
+int tg_gemm_tail_split(int64_t M, int64_t N, int64_t K, unsigned flags) {
+  if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return -TG_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR)) return -TG_ERR_UNSUPPORTED;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return -TG_ERR_CUDA;
+  return bf16_tail_split(M, N, K, (flags & TG_FLAG_CTA_PAIR) != 0, ctx);
+}
+
 int tg_skinny_split_count(int64_t N, int64_t K, int split_k) {
   if (N < 1 || K < 1 || split_k < 0 || N > kMaxDim || K > kMaxDim) return -TG_ERR_INVALID_ARG;
   DeviceCtx* ctx = current_ctx();
@@ -423,6 +475,8 @@ int tg_device_status(void* cuda_stream, uint32_t* site) {
   e = cudaMemcpyToSymbol(g_status_record, zero, sizeof(zero));
   if (e != cudaSuccess) return cuda_fail(e);
   if (site) *site = rec[1];
+  // A launch that gave up may have left tail-split flags set: start over.
+  if (rec[0] != TG_OK) reset_tail_flags();
   return static_cast<int>(rec[0]);
 }
 

@@ -62,6 +62,17 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
                   : launch_gemm_cfg<CfgPairF32>(tA, tB, tA, tB, a, stream, ctx);
 }
 
+int bf16_tail_split(int64_t M, int64_t N, int64_t K, bool pair, DeviceCtx* ctx) {
+  const int g = pair ? 2 : 1;
+  const int num_tiles = ceil_div_i(M, 128 * g) * ceil_div_i(N, 256);
+  const int units_max =
+      pair ? gemm_units_for_device<CfgPairF32>(ctx) : gemm_units_for_device<CfgF32>(ctx);
+  if (units_max < 0) return -TG_ERR_CUDA;
+  int W = 0, R = 0;
+  return pair ? tail_split_for<CfgPairF32>(num_tiles, ceil_div_i(K, 64), units_max, &W, &R)
+              : tail_split_for<CfgF32>(num_tiles, ceil_div_i(K, 64), units_max, &W, &R);
+}
+
 // ---------------------------------------------------------------------------
 // K == 0: D = epilogue(0)
 // ---------------------------------------------------------------------------

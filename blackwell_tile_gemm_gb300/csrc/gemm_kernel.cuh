@@ -46,6 +46,7 @@ enum : uint32_t {
   kSiteMmaAccEmpty = 3,
   kSiteEpiAccFull = 4,
   kSiteScaleFull = 5,
+  kSiteTailFlag = 6,
 };
 
 struct GemmArgs {
@@ -61,6 +62,17 @@ struct GemmArgs {
   int raster_group; // m-tiles per band of the tile order
   const int* gather_idx;  // gathered A: D row i uses A row gather_idx[i] (else null)
   int gather_rows;        // rows of A; indices outside [0, gather_rows) read zeros
+  // Tail split (see next_work): tiles below full_tiles are whole work items;
+  // with tail_split = S > 1 the tail_items = R * S items that follow are K
+  // pieces of the R last tiles.  Piece p > 0 writes its f32 partial tile to
+  // partials and sets its flag to 1; piece 0 waits for the flags, adds the
+  // partials before its epilogue and sets the flags back to 0, so that every
+  // launch (also a graph replay) starts from zeroed flags.
+  int full_tiles;
+  int tail_split;
+  int tail_items;
+  float* partials;        // [tail tile][piece-1][CTA of pair][BN cols][128 rows] f32
+  uint32_t* flags;        // [tail tile][piece-1][CTA of pair], 0 between launches
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -154,6 +166,48 @@ struct GemmCfg {
   static_assert(!kMx || BN % 128 == 0, "scale images cover 128-row blocks of B");
   static_assert(!kGather || (!kMx && !kMcast), "gathered A: bf16, without multicast");
 };
+
+// One work item of a unit: a whole tile, or one K piece of a tail tile.
+struct Work {
+  int t;        // tile id (tile order)
+  int k0, k1;   // K stages k0, k0 + ks, ... below k1
+  int ks;
+  int piece;    // K piece (0: the owner, which stores D)
+  int tail;     // tail tile index, or -1 for a whole tile
+};
+
+// Item i of `unit`: tiles unit, unit + U, ... below full_tiles; then, with a
+// tail split, the unit's one K piece of a tail tile.  Every unit runs full
+// waves of whole tiles (full_tiles = W * U), and the R tiles a last, partial
+// wave would leave to R units are cut into S pieces run by R * S units at
+// once.  All units of the grid are resident together, and only owners wait
+// (for pieces that never wait), so the pieces cannot block each other.
+__device__ __forceinline__ bool next_work(const GemmArgs& p, int unit, int num_units, int i,
+                                          Work& w) {
+  const int t = unit + i * num_units;
+  if (t < p.full_tiles) {
+    w.t = t;
+    w.k0 = 0;
+    w.k1 = p.num_k_blocks;
+    w.ks = 1;
+    w.piece = 0;
+    w.tail = -1;
+    return true;
+  }
+  if (p.tail_split <= 1 || i != p.full_tiles / num_units || unit >= p.tail_items) return false;
+  // Piece q takes stages q, q + S, q + 2S, ...: the S pieces of a tile then
+  // read neighbouring 128-byte chunks of each row at any moment.  (Pieces of
+  // contiguous K ranges kept fixed 2-4 KB offsets between them and ran 2-4x
+  // slower per SM, their loads landing on the same L2 slices.)
+  const int S = p.tail_split;
+  w.tail = unit / S;
+  w.piece = unit % S;
+  w.t = p.full_tiles + w.tail;
+  w.k0 = w.piece;
+  w.k1 = p.num_k_blocks;
+  w.ks = S;
+  return true;
+}
 
 // Grouped tile order: consecutive tile ids walk down a band of `group`
 // m-tiles before moving to the next n-tile, so the CTAs that run at the same
@@ -320,6 +374,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t* sf_drain_bar = sfr_bar + C::kStages;      // [kSfWarps] copies on give-up
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  // Tail split: epilogue warps done with their piece / done waiting as owner.
+  int* tail_count = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  int* owner_count = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
@@ -348,6 +405,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int w = 0; w < C::kSfWarps; ++w) mbar_init(&sf_drain_bar[w], 1);
     }
     *abort_flag = 0;
+    *tail_count = 0;
+    *owner_count = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -371,7 +430,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const WaitGuard guard{p.status, abort_flag, p.timeout_ns};
   // Work units: tiles of kPairs x 256 rows (one per cluster) by BN columns.
   const int num_mc = (p.num_m_tiles + C::kPairs - 1) / C::kPairs;
-  const int num_tiles = num_mc * p.num_n_tiles;
   const int unit = blockIdx.x / C::kClusterCtas;      // cluster index
   const int num_units = gridDim.x / C::kClusterCtas;
 
@@ -404,7 +462,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
-      for (int t = unit; t < num_tiles && ok; t += num_units) {
+      Work w;
+      for (int it = 0; ok && next_work(p, unit, num_units, it, w); ++it) {
+        const int t = w.t;
         int tmc, tn;
         tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
         const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
@@ -419,7 +479,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if (src < 0 || src >= p.gather_rows) src = p.gather_rows;
           r[j] = src;
         }
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = w.k0; kb < w.k1; kb += w.ks) {
           int got = 1;
           if (lane == 0)
             got = (mbar_try_wait(empty0 + 8u * stage, phase ^ 1u) ||
@@ -482,7 +542,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;   // per-stage bit masks
       bool ok = true;
-      for (int t = unit; t < num_tiles && ok; t += num_units) {
+      Work w;
+      for (int it = 0; ok && next_work(p, unit, num_units, it, w); ++it) {
+        const int t = w.t;
         int tmc, tn;
         tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
         const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
@@ -490,7 +552,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int b_row = tn * C::BN + static_cast<int>(pair_rank) * C::B_ROWS;
         const int sfa_row = C::kCtaGroup == 2 ? tm * 2 + static_cast<int>(pair_rank) : tm;
         const int sfb_row = tn * (C::BN / 128);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = w.k0; kb < w.k1; kb += w.ks) {
           if (!mbar_try_wait(empty0 + 8u * stage, phase ^ 1u) &&
               !mbar_wait(&empty_bar[stage], phase ^ 1u, guard, kSiteProducerEmpty)) {
             ok = false;
@@ -563,7 +625,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // its scales in TMEM (which that warp copies after the data landed).
       uint64_t* ready_bar = C::kMx ? sfr_bar : full_bar;
       const uint32_t ready0 = smem_addr(&ready_bar[0]);
-      for (int t = unit; t < num_tiles && ok; t += num_units) {
+      Work w;
+      for (int it = 0; ok && next_work(p, unit, num_units, it, w); ++it) {
         if (!mbar_try_wait(acce0 + 8u * acc, acc_phase ^ 1u) &&
             !mbar_wait(&acce_bar[acc], acc_phase ^ 1u, guard, kSiteMmaAccEmpty)) {
           ok = false;
@@ -571,7 +634,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = w.k0; kb < w.k1; kb += w.ks) {
           if (!ready && !mbar_try_wait(ready0 + 8u * stage, phase) &&
               !mbar_wait(&ready_bar[stage], phase, guard, kSiteMmaFull)) {
             ok = false;
@@ -593,14 +656,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               mma_block_scaled<C::kCtaGroup, C::kKind>(
                   d_tmem, ad + 2 * k, bd + 2 * k,
                   idesc_block_scaled<C::kKind>(C::MMA_M, C::BN, sf, sf), sfa_t + 4 * g,
-                  sfb_t + 4 * g * C::kSfBlocksB, (kb | k) != 0);
+                  sfb_t + 4 * g * C::kSfBlocksB, (kb != w.k0 || k != 0));
               if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           } else {
 #pragma unroll
             for (int k = 0; k < C::kIssues; ++k) {
               mma_bf16<C::kCtaGroup>(d_tmem, ad + 2 * k, bd + 2 * k,
-                                     idesc_bf16_f32(C::MMA_M, C::BN), (kb | k) != 0);
+                                     idesc_bf16_f32(C::MMA_M, C::BN), (kb != w.k0 || k != 0));
               if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           }
@@ -645,8 +708,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         uint32_t phase = 0;
         bool ok = true;
         bool copied = false;
-        for (int t = unit; t < num_tiles && ok; t += num_units) {
-          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        Work w;
+        for (int it = 0; ok && next_work(p, unit, num_units, it, w); ++it) {
+          for (int kb = w.k0; kb < w.k1; kb += w.ks) {
             if (!mbar_try_wait(full0 + 8u * stage, phase) &&
                 !mbar_wait(&full_bar[stage], phase, guard, kSiteScaleFull)) {
               ok = false;
@@ -690,9 +754,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     uint32_t acc_phase = 0;
     uint32_t acce_remote = 0;
     if constexpr (C::kCtaGroup == 2) acce_remote = map_to_cta(smem_addr(&acce_bar[0]), lead_rank);
-    for (int t = unit; t < num_tiles; t += num_units) {
+    Work w;
+    for (int it = 0; next_work(p, unit, num_units, it, w); ++it) {
       int tmc, tn;
-      tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
+      tile_coords(w.t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
       const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
       // One lane waits for the accumulator; the others wait at the warp barrier.
       int got = 1;
@@ -717,6 +782,66 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           mbar_arrive_relaxed(&acce_bar[acc]);
         else
           mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+      }
+      if (w.tail >= 0) {
+        // Tail split.  A partial tile is stored column-major, [BN][128] f32:
+        // the 32 lanes of a warp (32 consecutive rows) then write and read
+        // 128 contiguous bytes per column.  part_col(q) points at this
+        // thread's row in the first of its columns.
+        const int S1 = p.tail_split - 1;
+        auto part_col = [&](int piece) {
+          return p.partials +
+                 ((static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup + pair_rank) *
+                     (128 * C::BN) +
+                 static_cast<int64_t>(half * C::kEpiCols) * 128 + row_in_tile;
+        };
+        auto flag_of = [&](int piece) {
+          return p.flags + (static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup +
+                 pair_rank;
+        };
+        if (w.piece > 0) {
+          // A K piece: publish the raw f32 partial for the owner, store no D.
+          float* dst = part_col(w.piece);
+#pragma unroll
+          for (int c = 0; c < C::kEpiChunks; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) __stcg(dst + (32 * c + i) * 128, __uint_as_float(v[c][i]));
+          __threadfence();
+          __syncwarp();
+          // The last of the epilogue warps to finish releases the flag.
+          if (lane == 0 && atomicAdd(tail_count, 1) == C::kEpiWarps - 1) {
+            __threadfence();
+            flag_set_release(flag_of(w.piece), 1u);
+          }
+          if (++acc == C::kAccBufs) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          continue;
+        }
+        // The owner: wait for every other piece (bounded), then add them.
+        int ready = 1;
+        if (lane == 0)
+          for (int q = 1; q <= S1 && ready; ++q)
+            ready = flag_wait_eq(flag_of(q), 1u, guard, kSiteTailFlag) ? 1 : 0;
+        ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+        if (!ready) break;
+        for (int q = 1; q <= S1; ++q) {
+          uint32_t seen;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(flag_of(q)) : "memory");
+          (void)seen;
+          const float* src = part_col(q);
+#pragma unroll
+          for (int c = 0; c < C::kEpiChunks; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[c][i] = __float_as_uint(__uint_as_float(v[c][i]) + __ldcg(src + (32 * c + i) * 128));
+        }
+        // Once all eight epilogue warps have seen the flags, the last one
+        // sets them back to 0 for the next launch.
+        __syncwarp();
+        if (lane == 0 && atomicAdd(owner_count, 1) == C::kEpiWarps - 1)
+          for (int q = 1; q <= S1; ++q) flag_set_release(flag_of(q), 0u);
       }
       const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
       const int col_base = tn * C::BN + half * C::kEpiCols;

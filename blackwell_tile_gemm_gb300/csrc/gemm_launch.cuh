@@ -51,6 +51,29 @@ int gemm_units_for_device(DeviceCtx* ctx) {
   return units;
 }
 
+// Tail split of `num_tiles` tiles over `units_max` units (see GemmArgs):
+// returns S (1: none) and sets W (full waves) and R (tiles left over).
+template <class C>
+int tail_split_for(int num_tiles, int num_k_blocks, int units_max, int* W, int* R) {
+  *W = num_tiles / units_max;
+  *R = num_tiles - *W * units_max;
+  // Measured on GB300 (graph-replayed, per call): a split K over otherwise
+  // idle units pays off for dense bf16 when all tiles fit in half a wave
+  // (512 x 512 x 8192: 43 -> 30 us; 1024 x 1024 x 8192 in pairs: 45 -> 39
+  // us).  After full waves it gained nothing at 8192^3 (the units still busy
+  // in a partial wave run faster than in a full one), and for the
+  // block-scaled kinds the exchange of partial tiles cost more than it saved
+  // (1024 x 1024 x 8192 MXFP8: 29 -> 33 us).  So: dense kinds, W == 0 only.
+  if (C::kMcast || C::kMx || *W > 0 || *R == 0 || 2 * *R > units_max) return 1;
+  int S = units_max / *R;
+  if (S > 4) S = 4;
+  while (S >= 2 && num_k_blocks < 4 * S) --S;
+  const size_t bytes = static_cast<size_t>(*R) * (S - 1) * C::kCtaGroup * 128 * C::BN * 4;
+  if (S < 2 || bytes > kTailPartialBytes || *R * (S - 1) * C::kCtaGroup > kTailFlagWords)
+    return 1;
+  return S;
+}
+
 template <class C>
 int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tSFA,
                     const CUtensorMap& tSFB, const GemmArgs& args, cudaStream_t stream,
@@ -58,7 +81,30 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
   const int units_max = gemm_units_for_device<C>(ctx);
   if (units_max < 0) return TG_ERR_CUDA;
   const int num_tiles = (args.num_m_tiles + C::kPairs - 1) / C::kPairs * args.num_n_tiles;
-  const int units = num_tiles < units_max ? num_tiles : units_max;
+  int units = num_tiles < units_max ? num_tiles : units_max;
+  GemmArgs a = args;
+  a.full_tiles = num_tiles;
+  a.tail_split = 1;
+  a.tail_items = 0;
+  a.partials = nullptr;
+  a.flags = nullptr;
+  {
+    // Tail split: W full waves of whole tiles over all units; the R tiles of
+    // a last, partial wave are cut into S K-pieces (S <= units / R, at most
+    // 4, each piece at least 4 stages) so that R * S units finish together.
+    int W = 0, R = 0;
+    const int S = tail_split_for<C>(num_tiles, args.num_k_blocks, units_max, &W, &R);
+    float* part = nullptr;
+    uint32_t* flags = nullptr;
+    if (S >= 2 && tail_scratch(stream, &part, &flags)) {
+      a.full_tiles = W * units_max;
+      a.tail_split = S;
+      a.tail_items = R * S;
+      a.partials = part;
+      a.flags = flags;
+      units = W > 0 ? units_max : R * S;
+    }
+  }
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(static_cast<unsigned>(units * C::kClusterCtas), 1, 1);
@@ -73,7 +119,7 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, tA, tB, tSFA, tSFB, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, tA, tB, tSFA, tSFB, a);
   if (e != cudaSuccess) return cuda_fail(e);
   return TG_OK;
 }

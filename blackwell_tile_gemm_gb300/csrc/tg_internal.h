@@ -39,6 +39,23 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
 // long (grown on demand).  nullptr on failure.
 void* device_workspace(size_t bytes);
 
+// Scratch for the tail split of the persistent GEMM (partial tiles of the
+// last wave's K pieces, and their flags), one set per (device, stream) so
+// that calls on different streams never share it.  Allocated on the first
+// call that splits on that stream; the flags start at zero and every launch
+// leaves them at zero.  false if it cannot be had (the call then runs
+// without a split).
+constexpr size_t kTailPartialBytes = size_t{20} << 20;   // >= 152 slots of 128 KiB
+constexpr int kTailFlagWords = 1024;
+bool tail_scratch(cudaStream_t stream, float** partials, uint32_t** flags);
+// Zero the tail flags of the current device (after a device-side error, a
+// launch may have left some set).
+void reset_tail_flags();
+
+// Tail split (K pieces per leftover tile, 1 = none) the dense bf16 kernel
+// uses for this shape on the context's device; negative status on failure.
+int bf16_tail_split(int64_t M, int64_t N, int64_t K, bool pair, DeviceCtx* ctx);
+
 // Launchers (arguments already validated).  kind: kKindBf16 or a
 // block-scaled kind (gemm_kinds.h).
 int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -86,6 +86,19 @@ typedef struct tg_epilogue {
   const float* bias;
 } tg_epilogue;
 
+/*
+ * Tail split.  The GEMM kernels are persistent: every SM (or SM pair) walks
+ * its share of the output tiles.  When all R tiles of a dense (bf16) product
+ * fit in half a wave, each is cut into S pieces along K (S <= 4, S * R <=
+ * the co-resident units, pieces of >= 4 stages) that run at the same time;
+ * the pieces add their f32 partial tiles through a per-(device, stream)
+ * scratch of 20 MiB plus a flag block, allocated with cudaMalloc on the
+ * first call that splits on a stream (make that call before capturing the
+ * stream into a CUDA graph).  Results agree with the unsplit product within
+ * the tolerances above; the partials are added in a fixed order, so repeated
+ * calls give identical bits.
+ */
+
 /* Launch flags (bit set). */
 enum {
   TG_FLAG_CTA_PAIR = 1u, /* cta_group::2: two CTAs of a cluster share one
@@ -204,6 +217,11 @@ int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* 
                      int64_t K, int d_dtype, const tg_epilogue* epi, unsigned flags,
                      void* cuda_stream);
 
+/* tg_gemm_tail_split -- the number of K pieces (1: none) into which
+ * gemm_bf16 cuts each tile for this shape on the current device (flags: 0 or
+ * TG_FLAG_CTA_PAIR); minus a status code on failure.  See "Tail split". */
+int tg_gemm_tail_split(int64_t M, int64_t N, int64_t K, unsigned flags);
+
 /* tg_skinny_split_count -- the number of K pieces gemm_bf16_skinny uses for
  * (N, K, split_k) on the current device, or minus a status code. */
 int tg_skinny_split_count(int64_t N, int64_t K, int split_k);
@@ -291,7 +309,9 @@ int tile_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out,
  * pipeline wait passed its deadline (the kernel then stopped early, left its
  * outputs incomplete and released its tensor memory), or TG_ERR_CUDA when
  * the synchronisation itself failed.  `site` (may be NULL) receives the code
- * of the wait that expired.
+ * of the wait that expired.  After an error it also clears the library's
+ * cross-CTA flags on this device (see "Tail split" above); other streams of
+ * the device should be idle at that point.
  */
 int tg_device_status(void* cuda_stream, uint32_t* site);
 
