@@ -121,7 +121,6 @@ struct GemmCfg {
   static constexpr int OFF_B = OFF_A + kStages * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + kStages * SFA_BYTES;
-  static constexpr int OFF_BAR = (OFF_SFB + kStages * SFB_BYTES + 7) & ~7;
   // Block-scaled kinds: two warps copy the scales into TMEM, each issuing
   // half of a stage's tcgen05.cp.  A copy costs its issuing thread ~80
   // cycles before the next one issues, while copies from different warps
@@ -131,6 +130,18 @@ struct GemmCfg {
   static constexpr int kSfWarps = kMx ? 2 : 0;
   static constexpr int NUM_BARS =
       (kMx ? 3 : 2) * kStages + 2 * kAccBufs + 1 + kSfWarps;
+  // TMA-store epilogue, with two accumulator buffers and where shared
+  // memory allows: each epilogue warp stages 32 rows x 128 bytes (32 f32 or
+  // 64 bf16 columns) at a time, 128B swizzled, and one lane stores the box
+  // with TMA (full 128-byte lines).  The block-scaled rings (one accumulator,
+  // which their epilogue must hand back as early as possible) store from
+  // registers with st.global.v4.
+  static constexpr int OFF_SF_END = OFF_SFB + kStages * SFB_BYTES;
+  static constexpr int kStgWarpBytes = 32 * 128;
+  static constexpr int OFF_STG = (OFF_SF_END + 1023) & ~1023;
+  static constexpr bool kTmaStore =
+      kAccBufs == 2 && OFF_STG + 8 * kStgWarpBytes + NUM_BARS * 8 + 16 + 1024 <= 227 * 1024;
+  static constexpr int OFF_BAR = kTmaStore ? OFF_STG + 8 * kStgWarpBytes : ((OFF_SF_END + 7) & ~7);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   // tensor memory columns
@@ -355,12 +366,44 @@ __device__ __forceinline__ void epilogue_store_chunk(const GemmArgs& p, int row,
   }
 }
 
+// TMA-store epilogue: writes one 32-row x 128-byte box of D (lane = row)
+// into this warp's staging buffer, 128B-swizzled: 16-byte piece j of row r
+// sits at r*128 + ((j ^ (r & 7)) * 16), so the eight lanes of each quarter
+// warp write eight different bank groups.  The box holds 32 f32 columns
+// (chunk va) or 64 bf16 columns (chunks va, vb).  stg_row = buffer + lane*128.
+template <class C, bool kAdd>
+__device__ __forceinline__ void epilogue_stage_box(uint32_t stg_row, uint32_t lane,
+                                                   const uint32_t (&va)[32],
+                                                   const uint32_t (&vb)[32], float add) {
+  const uint32_t sw = lane & 7u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t w[4];
+    if constexpr (C::kBf16Out) {
+      const uint32_t(&src)[32] = j < 4 ? va : vb;
+      const int c0 = 8 * (j & 3);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = __uint_as_float(src[c0 + 2 * e]);
+        const float x1 = __uint_as_float(src[c0 + 2 * e + 1]);
+        w[e] = kAdd ? pack_bf16x2(x0 + add, x1 + add) : pack_bf16x2(x0, x1);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = kAdd ? __float_as_uint(__uint_as_float(va[4 * j + e]) + add) : va[4 * j + e];
+    }
+    st_shared_v4(stg_row + ((static_cast<uint32_t>(j) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA,
-                        const __grid_constant__ CUtensorMap tmSFB, const GemmArgs p) {
+                        const __grid_constant__ CUtensorMap tmSFB,
+                        const __grid_constant__ CUtensorMap tmD, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -416,6 +459,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       prefetch_tensormap(&tmSFA);
       prefetch_tensormap(&tmSFB);
     }
+    if constexpr (C::kTmaStore) prefetch_tensormap(&tmD);
   }
   if (warp == 1) {
     tmem_alloc<C::kCtaGroup>(tmem_slot, C::TMEM_COLS);
@@ -750,6 +794,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // transform the registers in place.
     const bool epi_lean = p.epi.op == kEpiNone || p.epi.op == kEpiAddScalar;
     const float epi_add = p.epi.op == kEpiAddScalar ? p.epi.alpha : 0.0f;
+    // This warp's staging buffer for the TMA-store epilogue.
+    const uint32_t stg =
+        smem_addr(smem + C::OFF_STG) + static_cast<uint32_t>(warp - 2) * C::kStgWarpBytes;
+    const uint32_t stg_row = stg + lane * 128u;
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t acce_remote = 0;
@@ -767,98 +815,221 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(slab * 32) << 16) +
                              static_cast<uint32_t>(acc * C::ACC_COLS + half * C::kEpiCols);
-      // Read this warp's whole share of the accumulator, then hand the
-      // accumulator back to the MMA warp before converting and storing.
-      uint32_t v[C::kEpiChunks][32];
+      // Tail split.  A partial tile is stored column-major, [BN][128] f32:
+      // the 32 lanes of a warp (32 consecutive rows) then write and read 128
+      // contiguous bytes per column.  part_col(q) points at this thread's row
+      // in the first of its columns; flag_of(q) is piece q's ready flag.
+      const int S1 = p.tail_split - 1;
+      auto part_col = [&](int piece) {
+        return p.partials +
+               ((static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup + pair_rank) *
+                   (128 * C::BN) +
+               static_cast<int64_t>(half * C::kEpiCols) * 128 + row_in_tile;
+      };
+      auto flag_of = [&](int piece) {
+        return p.flags + (static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup +
+               pair_rank;
+      };
+      if constexpr (C::kTmaStore) {
+        // Box-wise: the accumulator is read one box (32 rows x 128 bytes of
+        // D) at a time, which keeps 32 or 64 values live instead of 128; the
+        // second accumulator buffer lets the MMA warp run ahead meanwhile.
+        // The buffer goes back after its last read.
+        constexpr int kPerBox = C::kBf16Out ? 2 : 1;   // accumulator chunks per box
+        constexpr int kBoxes = C::kEpiChunks / kPerBox;
+        const bool tail_piece = w.tail >= 0 && w.piece > 0;
+        const bool tail_owner = w.tail >= 0 && w.piece == 0;
+        if (tail_owner) {
+          int ready = 1;
+          if (lane == 0)
+            for (int q = 1; q <= S1 && ready; ++q)
+              ready = flag_wait_eq(flag_of(q), 1u, guard, kSiteTailFlag) ? 1 : 0;
+          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+          if (!ready) break;
+          for (int q = 1; q <= S1; ++q) {
+            uint32_t seen;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                         : "=r"(seen)
+                         : "l"(flag_of(q))
+                         : "memory");
+            (void)seen;
+          }
+        }
+        const int row0 = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + slab * 32;
+        const int col_base = tn * C::BN + half * C::kEpiCols;
 #pragma unroll
-      for (int c = 0; c < C::kEpiChunks; ++c) tmem_ld_32x32b_x32(t_row + 32 * c, v[c]);
-      tmem_ld_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      // The reads are complete (wait::ld): a relaxed arrive hands the
-      // accumulator back without waiting for this warp's earlier D stores.
-      if (lane == 0) {
-        if constexpr (C::kCtaGroup == 1)
-          mbar_arrive_relaxed(&acce_bar[acc]);
-        else
-          mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
-      }
-      if (w.tail >= 0) {
-        // Tail split.  A partial tile is stored column-major, [BN][128] f32:
-        // the 32 lanes of a warp (32 consecutive rows) then write and read
-        // 128 contiguous bytes per column.  part_col(q) points at this
-        // thread's row in the first of its columns.
-        const int S1 = p.tail_split - 1;
-        auto part_col = [&](int piece) {
-          return p.partials +
-                 ((static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup + pair_rank) *
-                     (128 * C::BN) +
-                 static_cast<int64_t>(half * C::kEpiCols) * 128 + row_in_tile;
-        };
-        auto flag_of = [&](int piece) {
-          return p.flags + (static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup +
-                 pair_rank;
-        };
-        if (w.piece > 0) {
-          // A K piece: publish the raw f32 partial for the owner, store no D.
-          float* dst = part_col(w.piece);
+        for (int b = 0; b < kBoxes; ++b) {
+          uint32_t vb[kPerBox][32];
 #pragma unroll
-          for (int c = 0; c < C::kEpiChunks; ++c)
+          for (int h = 0; h < kPerBox; ++h)
+            tmem_ld_32x32b_x32(t_row + 32 * (kPerBox * b + h), vb[h]);
+          tmem_ld_wait();
+          if (b == kBoxes - 1) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (C::kCtaGroup == 1)
+                mbar_arrive_relaxed(&acce_bar[acc]);
+              else
+                mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+            }
+          }
+          if (tail_piece) {
+            float* dst = part_col(w.piece);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) __stcg(dst + (32 * c + i) * 128, __uint_as_float(v[c][i]));
+            for (int h = 0; h < kPerBox; ++h)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                __stcg(dst + (32 * (kPerBox * b + h) + i) * 128, __uint_as_float(vb[h][i]));
+            continue;
+          }
+          if (tail_owner)
+            for (int q = 1; q <= S1; ++q) {
+              const float* src = part_col(q);
+#pragma unroll
+              for (int h = 0; h < kPerBox; ++h)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  vb[h][i] = __float_as_uint(__uint_as_float(vb[h][i]) +
+                                             __ldcg(src + (32 * (kPerBox * b + h) + i) * 128));
+            }
+          const int col0 = col_base + 32 * kPerBox * b;
+          if (row0 < p.M && col0 < p.N) {
+            if (!epi_lean) {
+#pragma unroll
+              for (int h = 0; h < kPerBox; ++h)
+                if (col0 + 32 * h < p.N) epilogue_general_chunk(p, col0 + 32 * h, vb[h]);
+            }
+            if (col0 + 32 * kPerBox <= p.N) {
+              // The previous box's store has finished reading the buffer.
+              if (lane == 0) bulk_wait_group_read0();
+              __syncwarp();
+              if (epi_lean)
+                epilogue_stage_box<C, true>(stg_row, lane, vb[0], vb[kPerBox - 1], epi_add);
+              else
+                epilogue_stage_box<C, false>(stg_row, lane, vb[0], vb[kPerBox - 1], 0.0f);
+              fence_proxy_async_smem();
+              __syncwarp();
+              // Rows >= M are clipped by the store.
+              if (lane == 0) {
+                tma_store_2d_hint(&tmD, stg, col0, row0, pol_d);
+                bulk_commit_group();
+              }
+            } else {
+              // The box crosses column N: a clipped TMA store may write up to
+              // the next 16-byte boundary past N, into the caller's row
+              // padding, so the ragged box is stored from registers.
+              const int row = row0 + static_cast<int>(lane);
+#pragma unroll
+              for (int h = 0; h < kPerBox; ++h)
+                if (row < p.M && col0 + 32 * h < p.N) {
+                  if (epi_lean)
+                    epilogue_store_chunk<C, true>(p, row, col0 + 32 * h, vb[h], epi_add, pol_d);
+                  else
+                    epilogue_store_chunk<C, false>(p, row, col0 + 32 * h, vb[h], 0.0f, pol_d);
+                }
+            }
+          }
+        }
+        if (tail_piece) {
+          // Publish the partial: the last epilogue warp to finish sets the flag.
           __threadfence();
           __syncwarp();
-          // The last of the epilogue warps to finish releases the flag.
           if (lane == 0 && atomicAdd(tail_count, 1) == C::kEpiWarps - 1) {
             __threadfence();
             flag_set_release(flag_of(w.piece), 1u);
           }
-          if (++acc == C::kAccBufs) {
-            acc = 0;
-            acc_phase ^= 1u;
-          }
-          continue;
-        }
-        // The owner: wait for every other piece (bounded), then add them.
-        int ready = 1;
-        if (lane == 0)
-          for (int q = 1; q <= S1 && ready; ++q)
-            ready = flag_wait_eq(flag_of(q), 1u, guard, kSiteTailFlag) ? 1 : 0;
-        ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
-        if (!ready) break;
-        for (int q = 1; q <= S1; ++q) {
-          uint32_t seen;
-          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(flag_of(q)) : "memory");
-          (void)seen;
-          const float* src = part_col(q);
-#pragma unroll
-          for (int c = 0; c < C::kEpiChunks; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              v[c][i] = __float_as_uint(__uint_as_float(v[c][i]) + __ldcg(src + (32 * c + i) * 128));
-        }
-        // Once all eight epilogue warps have seen the flags, the last one
-        // sets them back to 0 for the next launch.
-        __syncwarp();
-        if (lane == 0 && atomicAdd(owner_count, 1) == C::kEpiWarps - 1)
-          for (int q = 1; q <= S1; ++q) flag_set_release(flag_of(q), 0u);
-      }
-      const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
-      const int col_base = tn * C::BN + half * C::kEpiCols;
-      if (epi_lean) {
-#pragma unroll
-        for (int c = 0; c < C::kEpiChunks; ++c) {
-          const int col0 = col_base + 32 * c;
-          if (row < p.M && col0 < p.N)
-            epilogue_store_chunk<C, true>(p, row, col0, v[c], epi_add, pol_d);
+        } else if (tail_owner) {
+          // Once all eight epilogue warps have seen the flags, the last one
+          // sets them back to 0 for the next launch.
+          __syncwarp();
+          if (lane == 0 && atomicAdd(owner_count, 1) == C::kEpiWarps - 1)
+            for (int q = 1; q <= S1; ++q) flag_set_release(flag_of(q), 0u);
         }
       } else {
+        // Read this warp's whole share of the accumulator, then hand the
+        // accumulator back to the MMA warp before converting and storing.
+        uint32_t v[C::kEpiChunks][32];
 #pragma unroll
-        for (int c = 0; c < C::kEpiChunks; ++c) {
-          const int col0 = col_base + 32 * c;
-          if (row < p.M && col0 < p.N) {
-            epilogue_general_chunk(p, col0, v[c]);
-            epilogue_store_chunk<C, false>(p, row, col0, v[c], 0.0f, pol_d);
+        for (int c = 0; c < C::kEpiChunks; ++c) tmem_ld_32x32b_x32(t_row + 32 * c, v[c]);
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        // The reads are complete (wait::ld): a relaxed arrive hands the
+        // accumulator back without waiting for this warp's earlier D stores.
+        if (lane == 0) {
+          if constexpr (C::kCtaGroup == 1)
+            mbar_arrive_relaxed(&acce_bar[acc]);
+          else
+            mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+        }
+        if (w.tail >= 0) {
+          if (w.piece > 0) {
+            // A K piece: publish the raw f32 partial for the owner, store no D.
+            float* dst = part_col(w.piece);
+#pragma unroll
+            for (int c = 0; c < C::kEpiChunks; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                __stcg(dst + (32 * c + i) * 128, __uint_as_float(v[c][i]));
+            __threadfence();
+            __syncwarp();
+            // The last of the epilogue warps to finish releases the flag.
+            if (lane == 0 && atomicAdd(tail_count, 1) == C::kEpiWarps - 1) {
+              __threadfence();
+              flag_set_release(flag_of(w.piece), 1u);
+            }
+            if (++acc == C::kAccBufs) {
+              acc = 0;
+              acc_phase ^= 1u;
+            }
+            continue;
+          }
+          // The owner: wait for every other piece (bounded), then add them.
+          int ready = 1;
+          if (lane == 0)
+            for (int q = 1; q <= S1 && ready; ++q)
+              ready = flag_wait_eq(flag_of(q), 1u, guard, kSiteTailFlag) ? 1 : 0;
+          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+          if (!ready) break;
+          for (int q = 1; q <= S1; ++q) {
+            uint32_t seen;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                         : "=r"(seen)
+                         : "l"(flag_of(q))
+                         : "memory");
+            (void)seen;
+            const float* src = part_col(q);
+#pragma unroll
+            for (int c = 0; c < C::kEpiChunks; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                v[c][i] = __float_as_uint(__uint_as_float(v[c][i]) +
+                                          __ldcg(src + (32 * c + i) * 128));
+          }
+          // Once all eight epilogue warps have seen the flags, the last one
+          // sets them back to 0 for the next launch.
+          __syncwarp();
+          if (lane == 0 && atomicAdd(owner_count, 1) == C::kEpiWarps - 1)
+            for (int q = 1; q <= S1; ++q) flag_set_release(flag_of(q), 0u);
+        }
+        const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
+        const int col_base = tn * C::BN + half * C::kEpiCols;
+        if (epi_lean) {
+#pragma unroll
+          for (int c = 0; c < C::kEpiChunks; ++c) {
+            const int col0 = col_base + 32 * c;
+            if (row < p.M && col0 < p.N)
+              epilogue_store_chunk<C, true>(p, row, col0, v[c], epi_add, pol_d);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::kEpiChunks; ++c) {
+            const int col0 = col_base + 32 * c;
+            if (row < p.M && col0 < p.N) {
+              epilogue_general_chunk(p, col0, v[c]);
+              epilogue_store_chunk<C, false>(p, row, col0, v[c], 0.0f, pol_d);
+            }
           }
         }
       }
@@ -867,6 +1038,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    // Stores still in flight finish before the block (and its shared
+    // memory) goes away.
+    if constexpr (C::kTmaStore)
+      if (lane == 0) bulk_wait_group0();
   }
 
   // ---------------------------------------------------------------- teardown

@@ -105,6 +105,17 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
       units = W > 0 ? units_max : R * S;
     }
   }
+  // D for the TMA-store epilogue: [M rows][N columns] at row stride ldd,
+  // boxes of 32 rows x 128 bytes (the API checks D's 16-byte alignment).
+  CUtensorMap tD = tA;
+  if constexpr (C::kTmaStore) {
+    const int esize = C::kBf16Out ? 2 : 4;
+    const int rc = make_tensor_map_2d(
+        &tD, C::kBf16Out ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+        args.D, static_cast<uint64_t>(args.N), static_cast<uint64_t>(args.M),
+        static_cast<uint64_t>(args.ldd) * esize, 128 / esize, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != TG_OK) return rc;
+  }
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(static_cast<unsigned>(units * C::kClusterCtas), 1, 1);
@@ -119,7 +130,7 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, tA, tB, tSFA, tSFB, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, tA, tB, tSFA, tSFB, tD, a);
   if (e != cudaSuccess) return cuda_fail(e);
   return TG_OK;
 }

@@ -374,8 +374,14 @@ int skinny_splits(int64_t N, int64_t K, int split_k, int num_sms, int* per_split
   return (total + per - 1) / per;   // no empty pieces
 }
 
+// f32 D is its own reduction target when its rows end on a 16-byte boundary
+// (N % 4 == 0).  A reduce whose box crosses a ragged column N may touch the
+// caller's row padding up to the next 16-byte boundary, so ragged f32 D and
+// bf16 D go through an f32 workspace of 16-byte rows and a finalize pass.
+bool skinny_direct(int64_t N, int d_dtype) { return d_dtype == TG_D_F32 && N % 4 == 0; }
+
 size_t skinny_workspace_bytes(int64_t M, int64_t N, int d_dtype, int epi_op) {
-  const bool direct = d_dtype == TG_D_F32;
+  const bool direct = skinny_direct(N, d_dtype);
   (void)epi_op;
   return direct ? 0 : static_cast<size_t>(M) * static_cast<size_t>((N + 3) / 4 * 4) * 4u;
 }
@@ -391,8 +397,7 @@ int launch_gemm_skinny_impl(const void* A, int64_t lda, const void* B, int64_t l
   a.scale = epi.op == kEpiAffine ? epi.alpha : 1.0f;
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
-  // f32 D is its own reduction target; bf16 D goes through an f32 workspace.
-  const bool direct = d_dtype == TG_D_F32;
+  const bool direct = skinny_direct(N, d_dtype);
   float* T = direct ? static_cast<float*>(D) : workspace;
   const int64_t ldt = direct ? ldd : (N + 3) / 4 * 4;
   const int64_t total = static_cast<int64_t>(M) * N;
@@ -430,7 +435,7 @@ int launch_gemm_skinny_impl(const void* A, int64_t lda, const void* B, int64_t l
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const float* Tc = T;
-    const int bf16_out = direct ? 0 : 1;
+    const int bf16_out = d_dtype == TG_D_BF16 ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, skinny_finalize_kernel, Tc, ldt, D, ldd, M, N, bf16_out, epi);
     if (e != cudaSuccess) return cuda_fail(e);
   }

@@ -81,10 +81,11 @@ def test_gather_out_of_range_indices_give_epilogue_of_zero(tg, oracle, pair, tma
 
 def test_gather_odd_k(tg, oracle):
     rng = np.random.default_rng(135)
-    a_rows, M, N, K = 90, 70, 40, 100          # K not a multiple of 8; lda padded to 104
-    A = np.zeros((a_rows, 104), np.uint16)
+    # K not a multiple of 8; lda padded to 104 with NaN, which no load may take.
+    a_rows, M, N, K = 90, 70, 40, 100
+    A = np.full((a_rows, 104), 0x7FC0, np.uint16)
     A[:, :K] = synth.bf16_uniform(rng, (a_rows, K))
-    B = np.zeros((N, 104), np.uint16)
+    B = np.full((N, 104), 0x7FC0, np.uint16)
     B[:, :K] = synth.bf16_uniform(rng, (N, K))
     torch = torch_cuda()
     idx = rng.integers(0, a_rows, M)

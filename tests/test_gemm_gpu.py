@@ -239,3 +239,62 @@ def test_mx8k_workload_sampled(tg, oracle):
     assert_within(got[rows], ref, mag, True, "mx8k rows")
     ref, mag = oracle.gemm_mxfp8(x["A"], x["B"], x["SFA"], x["SFB"], cols=cols)
     assert_within(got[:, cols], ref, mag, True, "mx8k cols")
+
+
+# ------------------------------------------------------- outside D, outside K
+
+@pytest.mark.parametrize("pair", [False, True, "mc"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 64), (37, 13, 72), (129, 250, 64), (260, 300, 200),
+                                   (300, 67, 128), (128, 192, 64)])
+def test_d_window_leaves_surroundings(tg, oracle, pair, out, M, N, K):
+    # D is a window of a NaN-filled buffer with 40 more rows and a padded row
+    # stride: the GEMM writes the window and nothing around it, whether the
+    # tile edge, the column edge N or a 16-byte boundary falls inside a box.
+    torch = torch_cuda()
+    rng = np.random.default_rng(M * 11 + N * 5 + K)
+    A, B = synth.bf16_uniform(rng, (M, K)), synth.bf16_uniform(rng, (N, K))
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    ldd = (N + 1 + 7) // 8 * 8
+    Dfull = torch.full((M + 40, ldd), float("nan"), dtype=dt, device="cuda")
+    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), Dfull[:M, :N], epilogue_add=1.0,
+                 cta_pair=bool(pair), multicast=pair == "mc")
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    got = host_values(Dfull)
+    ref, mag = oracle.gemm_bf16(A, B, add=1.0)
+    assert_within(got[:M, :N], ref, mag, out == "bf16", f"window {M}x{N}x{K}")
+    assert np.all(np.isnan(got[:M, N:])) and np.all(np.isnan(got[M:, :]))
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_mx_d_window_leaves_surroundings(tg, oracle, out):
+    torch = torch_cuda()
+    M, N, K = 140, 37, 96
+    x = synth.make_inputs("mx8k", M=M, N=N, K=K, seed=171)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    Dfull = torch.full((M + 40, 48), float("nan"), dtype=dt, device="cuda")
+    tg.gemm_mxfp8_blockscaled(dev_u8(x["A"]), dev_u8(x["B"]), dev_u8(x["SFA"]), dev_u8(x["SFB"]),
+                              Dfull[:M, :N])
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    got = host_values(Dfull)
+    ref, mag = oracle.gemm_mxfp8(x["A"], x["B"], x["SFA"], x["SFB"])
+    assert_within(got[:M, :N], ref, mag, out == "bf16", "mx window")
+    assert np.all(np.isnan(got[:M, N:])) and np.all(np.isnan(got[M:, :]))
+
+
+@pytest.mark.parametrize("pair", [False, True])
+def test_odd_k_never_reads_row_padding(tg, oracle, pair):
+    # K = 100 of a 104-element row stride; elements K..103 hold NaN, which
+    # would reach D if any load took them.
+    torch = torch_cuda()
+    rng = np.random.default_rng(172)
+    M, N, K = 200, 72, 100
+    A = np.full((M, 104), 0x7FC0, np.uint16)
+    B = np.full((N, 104), 0x7FC0, np.uint16)
+    A[:, :K] = synth.bf16_uniform(rng, (M, K))
+    B[:, :K] = synth.bf16_uniform(rng, (N, K))
+    D = torch.full((M, N), float("nan"), device="cuda")
+    tg.gemm_bf16(dev_bf16(A)[:, :K], dev_bf16(B)[:, :K], D, cta_pair=pair)
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    ref, mag = oracle.gemm_bf16(A[:, :K], B[:, :K])
+    assert_within(host_values(D), ref, mag, False, "odd K")

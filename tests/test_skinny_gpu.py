@@ -120,3 +120,39 @@ def test_skinny_8k_sampled(tg, oracle, M):
     cols = sample_indices(N, 128, 97, 128)
     ref, mag = oracle.gemm_bf16(A, B, cols=cols)
     assert_within(got[:, cols], ref, mag, True, f"skinny 8k M={M}")
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N", [(3, 13), (20, 130), (64, 257)])
+def test_d_window_leaves_surroundings(tg, oracle, out, M, N):
+    # D is a window of a buffer whose padding holds -0.0: neither a store nor
+    # a reduce-add (which would turn -0.0 into +0.0) may touch it.
+    torch = torch_cuda()
+    rng = np.random.default_rng(M * 13 + N)
+    K = 320
+    A, B = synth.bf16_uniform(rng, (M, K)), synth.bf16_uniform(rng, (N, K))
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    ldd = (N + 1 + 7) // 8 * 8
+    Dfull = torch.full((M + 8, ldd), -0.0, dtype=dt, device="cuda")
+    tg.gemm_bf16_skinny(dev_bf16(A), dev_bf16(B), Dfull[:M, :N], split_k=3)
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    got = host_values(Dfull)
+    ref, mag = oracle.gemm_bf16(A, B)
+    assert_within(got[:M, :N], ref, mag, out == "bf16", f"skinny window {M}x{N}")
+    for pad in (got[:M, N:], got[M:, :]):
+        assert np.all(pad == 0) and np.all(np.signbit(pad))
+
+
+def test_odd_k_never_reads_row_padding(tg, oracle):
+    torch = torch_cuda()
+    rng = np.random.default_rng(173)
+    M, N, K = 9, 200, 100
+    A = np.full((M, 104), 0x7FC0, np.uint16)
+    B = np.full((N, 104), 0x7FC0, np.uint16)
+    A[:, :K] = synth.bf16_uniform(rng, (M, K))
+    B[:, :K] = synth.bf16_uniform(rng, (N, K))
+    D = torch.full((M, N), float("nan"), device="cuda")
+    tg.gemm_bf16_skinny(dev_bf16(A)[:, :K], dev_bf16(B)[:, :K], D)
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    ref, mag = oracle.gemm_bf16(A[:, :K], B[:, :K])
+    assert_within(host_values(D), ref, mag, False, "skinny odd K")
