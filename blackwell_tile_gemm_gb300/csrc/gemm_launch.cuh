@@ -58,13 +58,13 @@ int tail_split_for(int num_tiles, int num_k_blocks, int units_max, int* W, int* 
   *W = num_tiles / units_max;
   *R = num_tiles - *W * units_max;
   // Measured on GB300 (graph-replayed, per call): a split K over otherwise
-  // idle units pays off for dense bf16 when all tiles fit in half a wave
-  // (512 x 512 x 8192: 43 -> 30 us; 1024 x 1024 x 8192 in pairs: 45 -> 39
-  // us).  After full waves it gained nothing at 8192^3 (the units still busy
-  // in a partial wave run faster than in a full one), and for the
-  // block-scaled kinds the exchange of partial tiles cost more than it saved
-  // (1024 x 1024 x 8192 MXFP8: 29 -> 33 us).  So: dense kinds, W == 0 only.
-  if (C::kMcast || C::kMx || *W > 0 || *R == 0 || 2 * *R > units_max) return 1;
+  // idle units pays off for dense bf16 when the last wave's tiles fill at
+  // most half of the units (512 x 512 x 8192: 43 -> 30 us; 1024 x 1024 x
+  // 8192 in pairs: 45 -> 39 us; after full waves 4096^3 93.5 -> 90.4 us,
+  // 8192^3 in pairs 654 -> 640 us).  For the block-scaled kinds the exchange
+  // of partial tiles cost more than it saved (1024 x 1024 x 8192 MXFP8:
+  // 29 -> 33 us).  So: dense kinds only.
+  if (C::kMcast || C::kMx || *R == 0 || 2 * *R > units_max) return 1;
   int S = units_max / *R;
   if (S > 4) S = 4;
   while (S >= 2 && num_k_blocks < 4 * S) --S;

@@ -88,9 +88,10 @@ typedef struct tg_epilogue {
 
 /*
  * Tail split.  The GEMM kernels are persistent: every SM (or SM pair) walks
- * its share of the output tiles.  When all R tiles of a dense (bf16) product
- * fit in half a wave, each is cut into S pieces along K (S <= 4, S * R <=
- * the co-resident units, pieces of >= 4 stages) that run at the same time;
+ * its share of the output tiles.  When the R tiles of a dense (bf16)
+ * product's last wave (after W >= 0 full waves over all co-resident units)
+ * fill at most half of the units, each of them is cut into S pieces along K
+ * (S <= 4, S * R <= the units, pieces of >= 4 stages) that run at the same time;
  * the pieces add their f32 partial tiles through a per-(device, stream)
  * scratch of 20 MiB plus a flag block, allocated with cudaMalloc on the
  * first call that splits on a stream (make that call before capturing the

@@ -1,6 +1,7 @@
-"""GPU parity of the tail split: when all tiles of a dense GEMM fit in half a
-wave of the persistent grid, each tile is cut into K pieces run by otherwise
-idle units, which add their f32 partial tiles for the piece that stores D.
+"""GPU parity of the tail split: when the tiles of a dense GEMM's last wave
+fill at most half of the persistent grid, each of them is cut into K pieces
+run by otherwise idle units, which add their f32 partial tiles for the piece
+that stores D.
 
 Shapes are chosen through tg_gemm_tail_split so that the split really
 happens on the device at hand.  Quarter-integer inputs keep every partial
@@ -137,6 +138,42 @@ def test_tail_split_gathered_rows(tg, oracle):
 
 
 def test_tail_split_query(tg):
-    assert tg.gemm_tail_split(8192, 8192, 8192, True) == 1     # full waves: no split
     assert tg.gemm_tail_split(128, 256, 64, False) == 1        # one tile, one stage
     assert tg.gemm_tail_split(512, 512, 8192, False) >= 2      # 8 tiles, long K
+    # One row of tiles, 1..400 of them: the split depends on the last wave
+    # only -- none where it fills more than half the units or is empty, one
+    # after full waves where it is small.
+    units = torch_cuda().cuda.get_device_properties(0).multi_processor_count
+    splits = [tg.gemm_tail_split(128, 256 * t, 8192, False) for t in range(1, 401)]
+    assert any(s == 1 for s in splits[units // 2 + 8:units - 8])
+    assert any(s >= 2 for s in splits[units + 8:])
+    assert all(1 <= s <= 4 for s in splits)
+
+
+@pytest.mark.parametrize("pair", [False, True])
+def test_tail_split_after_full_waves(tg, oracle, pair):
+    # More tiles than units, a small last wave split along K: full rows
+    # sampled from every 128-row block (all column tiles) match bit for bit.
+    torch = torch_cuda()
+    rng = np.random.default_rng(166 + pair)
+    K = 1024
+    units = torch.cuda.get_device_properties(0).multi_processor_count // (2 if pair else 1)
+    tm = 256 if pair else 128
+    shape = None
+    for nt in range(4, 40):
+        mt = units // nt + 1                              # just over one full wave
+        M, N = tm * mt, 256 * nt - 24
+        if mt * nt > units and tg.gemm_tail_split(M, N, K, pair) >= 2:
+            shape = (M, N)
+            break
+    if shape is None:
+        pytest.skip("no split-after-full-waves shape on this device")
+    M, N = shape
+    A, B = quarter_bits(rng, (M, K)), quarter_bits(rng, (N, K))
+    D = torch.full((M, N), float("nan"), device="cuda")
+    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), D, cta_pair=pair)
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    rows = np.unique(np.concatenate([np.arange(0, M, 128), np.arange(127, M, 128),
+                                     rng.integers(0, M, 32)]))
+    ref, _ = oracle.gemm_bf16(A, B, rows=rows)
+    assert np.array_equal(host_values(D)[rows], ref), f"{M}x{N}x{K}"
