@@ -94,6 +94,8 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(tg_epilogue), u32, vp]
         L.tg_gemm_tail_split.restype = i32
         L.tg_gemm_tail_split.argtypes = [i64, i64, i64, u32]
+        L.tg_gemm_repitch.restype = i32
+        L.tg_gemm_repitch.argtypes = [i64, i64, i64, i64, i64]
         L.tg_skinny_split_count.restype = i32
         L.tg_skinny_split_count.argtypes = [i64, i64, i32]
         for name in ("gemm_mxfp4_blockscaled", "gemm_nvfp4_blockscaled"):
@@ -331,6 +333,14 @@ def gemm_tail_split(M: int, N: int, K: int, cta_pair: bool = False) -> int:
     r = lib().tg_gemm_tail_split(int(M), int(N), int(K), TG_FLAG_CTA_PAIR if cta_pair else 0)
     if r < 0:
         raise TgError(-r, "tg_gemm_tail_split")
+    return r
+
+
+def gemm_repitch(M: int, N: int, K: int, lda: int, ldb: int) -> int:
+    """Operands gemm_bf16 copies to a 128-byte row pitch first: bit 0 A, bit 1 B."""
+    r = lib().tg_gemm_repitch(int(M), int(N), int(K), int(lda), int(ldb))
+    if r < 0:
+        raise TgError(-r, "tg_gemm_repitch")
     return r
 
 

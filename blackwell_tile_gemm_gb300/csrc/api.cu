@@ -36,7 +36,9 @@ struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
 };
-Workspace g_workspace[kMaxDevices];
+// One workspace per (device, stream): calls on different streams never
+// share one, and calls on one stream are ordered.
+std::map<std::pair<int, uintptr_t>, Workspace> g_workspace;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -159,15 +161,20 @@ void reset_tail_flags() {
     if (kv.first.first == dev) cudaMemset(kv.second.flags, 0, kTailFlagWords * sizeof(uint32_t));
 }
 
-void* device_workspace(size_t bytes) {
+void* device_workspace(size_t bytes, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mutex);
-  Workspace& w = g_workspace[dev];
+  Workspace& w = g_workspace[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
   if (w.bytes >= bytes && w.ptr) return w.ptr;
   if (w.ptr) {
-    // Earlier work on any stream may still read the old buffer.
-    if (cudaDeviceSynchronize() != cudaSuccess) return nullptr;
+    // Earlier work on this stream may still read the old buffer (a stream
+    // being captured cannot be synchronised: the call fails).
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+      cuda_fail(e);
+      return nullptr;
+    }
     cudaFree(w.ptr);
     w.ptr = nullptr;
     w.bytes = 0;
@@ -191,12 +198,21 @@ int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb
   if (K == 0) return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi, stream);
   const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
   const bool mcast = (flags & TG_FLAG_MULTICAST) != 0;
-  if (kind == kKindBf16)
+  if (kind == kKindBf16) {
+    const Bf16Repitch rp = bf16_repitch_plan(lda, ldb, M, N, K);
+    if (rp.bytes != 0) {
+      void* ws = device_workspace(rp.bytes, stream);
+      if (ws == nullptr) return TG_ERR_CUDA;
+      return launch_gemm_bf16_repitched(rp, A, lda, B, ldb, D, ldd, static_cast<int>(M),
+                                        static_cast<int>(N), static_cast<int>(K), d_dtype, epi,
+                                        pair, mcast, ws, stream, ctx);
+    }
     return launch_gemm_bf16_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M),
                                  static_cast<int>(N), static_cast<int>(K), d_dtype, epi, pair,
                                  mcast, stream, ctx);
+  }
   uint8_t* ws = static_cast<uint8_t*>(
-      device_workspace(blockscaled_workspace_bytes(kind, M, N, K, pair)));
+      device_workspace(blockscaled_workspace_bytes(kind, M, N, K, pair), stream));
   if (ws == nullptr) return TG_ERR_CUDA;
   return launch_gemm_blockscaled_impl(kind, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
                                       static_cast<int>(M), static_cast<int>(N),
@@ -373,7 +389,7 @@ int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, voi
   float* ws = nullptr;
   const size_t ws_bytes = skinny_workspace_bytes(M, N, d_dtype, e.op);
   if (ws_bytes) {
-    ws = static_cast<float*>(device_workspace(ws_bytes));
+    ws = static_cast<float*>(device_workspace(ws_bytes, stream));
     if (ws == nullptr) return TG_ERR_CUDA;
   }
   return launch_gemm_skinny_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M), static_cast<int>(N),
@@ -405,7 +421,7 @@ int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* 
     return launch_gemm_bf16_gather_impl(A, lda, static_cast<int>(a_rows), row_idx,
                                         static_cast<int>(M), B, ldb, D, ldd, static_cast<int>(N),
                                         static_cast<int>(K), d_dtype, e, pair, stream, ctx);
-  void* ws = device_workspace(gather_workspace_bytes(M, K));
+  void* ws = device_workspace(gather_workspace_bytes(M, K), stream);
   if (ws == nullptr) return TG_ERR_CUDA;
   return launch_gemm_bf16_pregather_impl(A, lda, static_cast<int>(a_rows), row_idx,
                                          static_cast<int>(M), B, ldb, D, ldd, static_cast<int>(N),
@@ -419,6 +435,12 @@ int tg_gemm_tail_split(int64_t M, int64_t N, int64_t K, unsigned flags) {
   DeviceCtx* ctx = current_ctx();
   if (!ctx) return -TG_ERR_CUDA;
   return bf16_tail_split(M, N, K, (flags & TG_FLAG_CTA_PAIR) != 0, ctx);
+}
+
+int tg_gemm_repitch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
+  if (M < 0 || N < 0 || K < 0 || lda < 0 || ldb < 0) return -TG_ERR_INVALID_ARG;
+  const Bf16Repitch rp = bf16_repitch_plan(lda, ldb, M, N, K);
+  return (rp.a ? 1 : 0) | (rp.b ? 2 : 0);
 }
 
 int tg_skinny_split_count(int64_t N, int64_t K, int split_k) {

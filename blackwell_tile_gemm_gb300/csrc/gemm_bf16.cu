@@ -74,6 +74,100 @@ int bf16_tail_split(int64_t M, int64_t N, int64_t K, bool pair, DeviceCtx* ctx) 
 }
 
 // ---------------------------------------------------------------------------
+// Re-pitch.  Measured on GB300 (4000 x 3000 x 1000, graph replay): rows of
+// 2000 bytes (16-byte aligned) 37.5 us, 2016 (32-byte) 30.6 us, 1984
+// (64-byte) 27.1 us, 2048 (128-byte) 26.8 us: a 128-byte box row that
+// straddles L2 lines lands late.  Copying A (and B) to rows of a 128-byte
+// pitch costs ~4 bytes per element of HBM or L2 traffic; for 16-byte rows
+// it pays when the product is large against its operands, M*N/(M+N) >=
+// 1250.  For 32-byte rows the copy cost more than it saved (8192^2 x 1000,
+// 2016-byte rows: 108 -> 118 us).
+
+namespace {
+
+// Rows [0, a_rows) come from A, the next b_rows from B, one warp per row:
+// exactly K elements (16-byte vectors, four per lane in flight, then the
+// last K % 8 one by one), so that nothing past column K is read.
+__global__ void repitch_rows_kernel(const uint16_t* __restrict__ a, int64_t lda, int a_rows,
+                                    const uint16_t* __restrict__ b, int64_t ldb, int b_rows,
+                                    uint16_t* __restrict__ dst, int64_t ld_dst, int K) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t total = static_cast<int64_t>(a_rows) + b_rows;
+  const int kv = K / 8;
+  for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < total; r += warps) {
+    const bool from_a = r < a_rows;
+    const uint16_t* s = from_a ? a + r * lda : b + (r - a_rows) * ldb;
+    uint16_t* d = dst + r * ld_dst;
+    const uint4* sv = reinterpret_cast<const uint4*>(s);
+    uint4* dv = reinterpret_cast<uint4*>(d);
+    for (int k0 = 0; k0 < kv; k0 += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + 32 * u + lane;
+        if (k < kv) v[u] = __ldcs(sv + k);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + 32 * u + lane;
+        if (k < kv) dv[k] = v[u];
+      }
+    }
+    const int t = kv * 8 + lane;
+    if (lane < 8 && t < K) d[t] = s[t];
+  }
+}
+
+// 0: rows 64-byte aligned (or better); else the alignment class in bytes.
+int row_alignment_class(int64_t ld) {
+  const int64_t b = ld * 2;
+  return b % 64 == 0 ? 0 : b % 32 == 0 ? 32 : 16;
+}
+
+}  // namespace
+
+Bf16Repitch bf16_repitch_plan(int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K) {
+  Bf16Repitch rp;
+  if (K < 128 || M <= 0 || N <= 0) return rp;
+  const double ratio = static_cast<double>(M) * static_cast<double>(N) / static_cast<double>(M + N);
+  auto wants = [&](int64_t ld) { return row_alignment_class(ld) == 16 && ratio >= 1250.0; };
+  rp.a = wants(lda);
+  rp.b = wants(ldb);
+  if (!rp.a && !rp.b) return rp;
+  rp.kp = (K + 63) / 64 * 64;
+  rp.bytes = static_cast<size_t>((rp.a ? M : 0) + (rp.b ? N : 0)) * static_cast<size_t>(rp.kp) * 2u;
+  return rp;
+}
+
+int launch_gemm_bf16_repitched(const Bf16Repitch& rp, const void* A, int64_t lda, const void* B,
+                               int64_t ldb, void* D, int64_t ldd, int M, int N, int K,
+                               int d_dtype, const Epi& epi, bool pair, bool mcast,
+                               void* workspace, cudaStream_t stream, DeviceCtx* ctx) {
+  // Workspace: A's rows (if re-pitched), then B's, each kp elements.
+  uint16_t* w = static_cast<uint16_t*>(workspace);
+  const int a_rows = rp.a ? M : 0, b_rows = rp.b ? N : 0;
+  int64_t blocks = (static_cast<int64_t>(a_rows) + b_rows + 7) / 8;
+  if (blocks > 16 * static_cast<int64_t>(ctx->num_sms)) blocks = 16 * ctx->num_sms;
+  repitch_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(A), lda, a_rows, static_cast<const uint16_t*>(B), ldb, b_rows,
+      w, rp.kp, K);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (rp.a) {
+    A = w;
+    lda = rp.kp;
+  }
+  if (rp.b) {
+    B = w + static_cast<int64_t>(a_rows) * rp.kp;
+    ldb = rp.kp;
+  }
+  return launch_gemm_bf16_impl(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epi, pair, mcast,
+                               stream, ctx);
+}
+
+// ---------------------------------------------------------------------------
 // K == 0: D = epilogue(0)
 // ---------------------------------------------------------------------------
 

@@ -31,38 +31,46 @@ using CfgGatherPairBf16 = GemmCfg<2, kKindBf16, 256, 2, 6, true, false, true>;
 // Row gather into a contiguous buffer: G[i, :] = A[idx[i], :] (zero rows for
 // indices outside A).  One warp per row, 16-byte vectors (K % 8 == 0 and a
 // 16-byte row stride, which the TMA row-stride rule already requires).
-__global__ void gather_rows_kernel(const uint4* __restrict__ A, int64_t lda_v, int a_rows,
-                                   const int* __restrict__ idx, int M, uint4* __restrict__ G,
-                                   int64_t ldg_v, int64_t row_v) {
+// One warp per gathered row: exactly K elements (16-byte vectors, then the
+// last K % 8 one by one), so nothing past column K of A is read.
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ A, int64_t lda, int a_rows,
+                                   const int* __restrict__ idx, int M, uint16_t* __restrict__ G,
+                                   int64_t ldg, int K) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int kv = K / 8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
        i < M; i += warps) {
     const int src = __ldg(idx + i);
     const bool valid = src >= 0 && src < a_rows;
-    const uint4* a = A + static_cast<int64_t>(valid ? src : 0) * lda_v;
-    uint4* g = G + i * ldg_v;
-    for (int64_t k = lane; k < row_v; k += 32)
-      g[k] = valid ? __ldg(a + k) : make_uint4(0u, 0u, 0u, 0u);
+    const uint16_t* a = A + static_cast<int64_t>(valid ? src : 0) * lda;
+    uint16_t* g = G + i * ldg;
+    const uint4* av = reinterpret_cast<const uint4*>(a);
+    uint4* gv = reinterpret_cast<uint4*>(g);
+    for (int k = lane; k < kv; k += 32) gv[k] = valid ? __ldg(av + k) : make_uint4(0u, 0u, 0u, 0u);
+    const int t = kv * 8 + lane;
+    if (lane < 8 && t < K) g[t] = valid ? a[t] : static_cast<uint16_t>(0);
   }
 }
 
 }  // namespace
 
+// Gathered rows are written at a 128-byte pitch: TMA boxes over rows that
+// are only 16-byte aligned land markedly slower.
 size_t gather_workspace_bytes(int64_t M, int64_t K) {
-  return static_cast<size_t>(M) * static_cast<size_t>((K + 7) / 8 * 8) * 2u;
+  return static_cast<size_t>(M) * static_cast<size_t>((K + 63) / 64 * 64) * 2u;
 }
 
 int launch_gemm_bf16_pregather_impl(const void* A, int64_t lda, int a_rows, const int* row_idx,
                                     int M, const void* B, int64_t ldb, void* D, int64_t ldd,
                                     int N, int K, int d_dtype, const Epi& epi, bool pair,
                                     void* workspace, cudaStream_t stream, DeviceCtx* ctx) {
-  const int64_t ldg = (K + 7) / 8 * 8;
+  const int64_t ldg = (K + 63) / 64 * 64;
   int64_t blocks = (static_cast<int64_t>(M) + 7) / 8;
   if (blocks > 16 * static_cast<int64_t>(ctx->num_sms)) blocks = 16 * ctx->num_sms;
   gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const uint4*>(A), lda / 8, a_rows, row_idx, M, static_cast<uint4*>(workspace),
-      ldg / 8, (K + 7) / 8);
+      static_cast<const uint16_t*>(A), lda, a_rows, row_idx, M,
+      static_cast<uint16_t*>(workspace), ldg, K);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return launch_gemm_bf16_impl(workspace, ldg, B, ldb, D, ldd, M, N, K, d_dtype, epi, pair, false,

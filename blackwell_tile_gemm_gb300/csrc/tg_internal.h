@@ -35,9 +35,11 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
                        uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                        uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
-// Library-owned device workspace for the current device, at least `bytes`
-// long (grown on demand).  nullptr on failure.
-void* device_workspace(size_t bytes);
+// Library-owned device workspace for (current device, `stream`), at least
+// `bytes` long (grown on demand: growing synchronises the stream first, so
+// make the largest call on a stream before capturing it into a graph).
+// nullptr on failure.
+void* device_workspace(size_t bytes, cudaStream_t stream);
 
 // Scratch for the tail split of the persistent GEMM (partial tiles of the
 // last wave's K pieces, and their flags), one set per (device, stream) so
@@ -69,6 +71,21 @@ int check_epilogue(const tg_epilogue* epi, Epi* out);
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
                           int64_t ldd, int M, int N, int K, int d_dtype, const Epi& epi,
                           bool pair, bool mcast, cudaStream_t stream, DeviceCtx* ctx);
+
+// Re-pitch of dense bf16 operands (gemm_bf16.cu).  TMA boxes over rows that
+// start only 16 bytes aligned straddle extra L2 lines and land ~40% slower;
+// for products large enough to repay a copy, such operands are first copied
+// into workspace rows of `kp` elements (128-byte pitch).
+struct Bf16Repitch {
+  bool a = false, b = false;
+  int64_t kp = 0;
+  size_t bytes = 0;  // workspace bytes; 0: no re-pitch
+};
+Bf16Repitch bf16_repitch_plan(int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K);
+int launch_gemm_bf16_repitched(const Bf16Repitch& rp, const void* A, int64_t lda, const void* B,
+                               int64_t ldb, void* D, int64_t ldd, int M, int N, int K,
+                               int d_dtype, const Epi& epi, bool pair, bool mcast,
+                               void* workspace, cudaStream_t stream, DeviceCtx* ctx);
 
 int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,

@@ -19,10 +19,14 @@
  *          applied to each register element before the store.
  *
  * Conventions shared by every call:
- *   - Ownership: the caller allocates and owns every buffer.  The library
- *     allocates no device memory for bf16 GEMM or the transpose; the MXFP8
- *     call keeps one library-owned scale-image workspace per device (grown
- *     on demand, never shrunk, freed at process exit).
+ *   - Ownership: the caller allocates and owns every buffer it passes.  The
+ *     library keeps its own workspace per (device, stream) -- scale images
+ *     of the block-scaled calls, gathered or re-pitched rows, the skinny
+ *     call's f32 partial sums -- allocated on the first call on a stream
+ *     that needs it, grown on demand (growing synchronises that stream, so
+ *     make the largest call on a stream before capturing it into a graph),
+ *     never shrunk, freed at process exit.  Calls on different streams never
+ *     share workspace.  The transpose allocates nothing.
  *   - Strides are in ELEMENTS and describe row-major 2-D arrays (unit inner
  *     stride).  Pointers are device pointers and must be 16-byte aligned;
  *     every row stride times the element size must be a multiple of 16 bytes.
@@ -130,6 +134,11 @@ enum {
  *          (TG_FLAG_MULTICAST alone: TG_ERR_INVALID_ARG).
  * Rounding: f32 -> bf16 D is round-to-nearest-even.  Alignment: A, B, D
  * 16-byte aligned; lda*2, ldb*2, ldd*sizeof(D) multiples of 16.
+ * Re-pitch: when lda*2 (or ldb*2) is not a multiple of 32 (rows only 16-byte
+ * aligned) and the product is large against its operands (M*N/(M+N) >=
+ * 1250), that operand is first copied into the stream's library workspace
+ * at a 128-byte pitch (ceil(K/64)*64 elements per row; K elements read per
+ * row); the result is the same, bit for bit.
  * Returns TG_OK once the kernel is enqueued, else an error (nothing enqueued).
  */
 int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
@@ -158,10 +167,9 @@ int gemm_bf16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, void* D
  *   K must be a multiple of 32 (one scale per 32 K elements); otherwise
  *   TG_ERR_INVALID_ARG.  lda and ldb must be multiples of 16.
  * The scales are first rearranged on the device into the tensor-memory image
- * the MMA reads (row r -> lane r%32, byte column 4*(r/32)) in a library-owned
- * per-device workspace of ceil(M/128)*ceil(K/128)*512 + ceil(N/128)*
- * ceil(K/128)*512 bytes; calls that overlap in time on different streams of
- * one device share that workspace and must not be issued concurrently.
+ * the MMA reads (row r -> lane r%32, byte column 4*(r/32)) in the stream's
+ * library workspace (ceil(M/128)*ceil(K/128)*512 + ceil(N/128)*
+ * ceil(K/128)*512 bytes).
  */
 int gemm_mxfp8_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
@@ -187,9 +195,9 @@ int gemm_mxfp8_blockscaled_ex(const void* A, int64_t lda, const void* B, int64_t
  *   M > 128: TG_ERR_UNSUPPORTED; split_k < 0: TG_ERR_INVALID_ARG.
  * With more than one piece the partial sums are added in a run-dependent
  * order, so the last bits of D may differ between runs.  bf16 D, and f32 D
- * with a SiLU epilogue, take one extra elementwise pass; bf16 D uses the
- * library workspace (M * ceil(N/4)*4 * 4 bytes), with the same rule on
- * concurrent calls as the block-scaled calls.
+ * with a SiLU epilogue, take one extra elementwise pass, and so does f32 D
+ * with N % 4 != 0; those cases use the stream's library workspace
+ * (M * ceil(N/4)*4 * 4 bytes).
  */
 int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
                      int64_t M, int64_t N, int64_t K, int d_dtype, const tg_epilogue* epi,
@@ -206,9 +214,9 @@ int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, voi
  *   flags   : TG_FLAG_CTA_PAIR and / or TG_FLAG_GATHER_TMA (TG_FLAG_MULTICAST:
  *             TG_ERR_UNSUPPORTED).
  *   K > 0 with a NULL row_idx or a_rows == 0: TG_ERR_INVALID_ARG.
- * By default the rows are first gathered into the library workspace
- * (M * ceil(K/8)*8 * 2 bytes; same rule on concurrent calls as the
- * block-scaled calls) and the dense kernel runs on them.  With
+ * By default the rows are first gathered into the stream's library
+ * workspace (M * ceil(K/64)*64 * 2 bytes: rows at a 128-byte pitch) and the
+ * dense kernel runs on them.  With
  * TG_FLAG_GATHER_TMA the GEMM loads them itself with tile::gather4 (no
  * workspace); that issue rate bounds it at ~60% of the dense kernel for
  * 4096 x 8192 x 8192.
@@ -222,6 +230,12 @@ int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* 
  * gemm_bf16 cuts each tile for this shape on the current device (flags: 0 or
  * TG_FLAG_CTA_PAIR); minus a status code on failure.  See "Tail split". */
 int tg_gemm_tail_split(int64_t M, int64_t N, int64_t K, unsigned flags);
+
+/* tg_gemm_repitch -- which operands gemm_bf16 / gemm_bf16_ex re-pitch for
+ * this shape and these row strides (see gemm_bf16): bit 0 A, bit 1 B (0:
+ * neither); minus TG_ERR_INVALID_ARG for negative sizes.  Host arithmetic
+ * only: no CUDA call, no device needed. */
+int tg_gemm_repitch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb);
 
 /* tg_skinny_split_count -- the number of K pieces gemm_bf16_skinny uses for
  * (N, K, split_k) on the current device, or minus a status code. */
@@ -240,9 +254,9 @@ int tg_skinny_split_count(int64_t N, int64_t K, int split_k);
  *   D, ldd, d_dtype, epi, flags: as for gemm_bf16_ex.
  *   K must be a multiple of 32; otherwise TG_ERR_INVALID_ARG.  lda >= K/2,
  *   ldb >= K/2, both multiples of 16 (TG_ERR_MISALIGNED).
- * The scales are rearranged into the tensor-memory image in the same
- * library-owned workspace as gemm_mxfp8_blockscaled (two 512-byte images per
- * 128 rows and 256 K), with the same rule on concurrent calls.
+ * The scales are rearranged into the tensor-memory image in the stream's
+ * library workspace, as for gemm_mxfp8_blockscaled (two 512-byte images per
+ * 128 rows and 256 K).
  */
 int gemm_mxfp4_blockscaled(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,

@@ -174,3 +174,21 @@ def test_gather_rejects_before_launch(L):
     # TG_FLAG_GATHER_TMA belongs to the gather call only
     assert L.gemm_bf16(A16, 64, A16, 64, A16, 64, 64, 64, 64, 0, 0, 0.0, 4, None) \
         == tg.TG_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape,lds,want", [
+    ((4000, 3000, 1000), (1000, 1000), 3),   # 16-byte rows, M*N/(M+N) = 1714
+    ((4000, 3000, 1000), (1024, 1024), 0),   # 128-byte rows
+    ((4000, 3000, 1000), (1000, 1024), 1),   # only A
+    ((4000, 3000, 992), (992, 1000), 2),     # 64-byte rows of A are fine
+    ((2048, 2048, 1000), (1000, 1000), 0),   # 1024 < 1250: the copy would not pay
+    ((8192, 8192, 1000), (1008, 1008), 0),   # 32-byte rows: never
+    ((8192, 8192, 1000), (1000, 1008), 1),
+    ((4000, 3000, 104), (104, 104), 0),      # K < 128
+])
+def test_repitch_rule(L, shape, lds, want):
+    assert tg.gemm_repitch(*shape, *lds) == want
+
+
+def test_repitch_rejects_negative_sizes(L):
+    assert L.tg_gemm_repitch(-1, 8, 8, 8, 8) == -tg.TG_ERR_INVALID_ARG

@@ -147,11 +147,79 @@ def test_repeat_runs_are_bit_identical(tg):
 
 
 def test_ragged_workload_full(tg, oracle):
-    # M=4000, N=3000, K=1000, D = A B^T + 1 in f32, every element.
+    # M=4000, N=3000, K=1000, D = A B^T + 1 in f32, every element.  Rows of
+    # 2000 bytes: both operands take the re-pitch copy first.
     x = synth.make_inputs("ragged")
+    assert tg.gemm_repitch(4000, 3000, 1000, 1000, 1000) == 3
     D = run_bf16(tg, x["A"], x["B"], "f32", add=1.0)
     ref, mag = oracle.gemm_bf16(x["A"], x["B"], add=1.0)
     assert_within(host_values(D), ref, mag, False, "ragged 4000x3000x1000")
+
+
+@pytest.mark.parametrize("pair", [False, True])
+def test_repitch_matches_aligned_strides_bit_for_bit(tg, pair):
+    # The same operands at lda = 1000 (re-pitched) and lda = 1024 (used in
+    # place) give the same bits: the copy changes where rows live, not the
+    # arithmetic.
+    torch = torch_cuda()
+    x = synth.make_inputs("ragged")
+    M, N, K = 4000, 3000, 1000
+    assert tg.gemm_repitch(M, N, K, 1024, 1024) == 0
+    Ap = torch.zeros((M, 1024), dtype=torch.bfloat16, device="cuda")
+    Bp = torch.zeros((N, 1024), dtype=torch.bfloat16, device="cuda")
+    Ap[:, :K] = dev_bf16(x["A"])
+    Bp[:, :K] = dev_bf16(x["B"])
+    D1 = torch.full((M, N), float("nan"), device="cuda")
+    D2 = torch.full((M, N), float("nan"), device="cuda")
+    tg.gemm_bf16(dev_bf16(x["A"]), dev_bf16(x["B"]), D1, epilogue_add=1.0, cta_pair=pair)
+    tg.gemm_bf16(Ap[:, :K], Bp[:, :K], D2, epilogue_add=1.0, cta_pair=pair)
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    assert torch.equal(D1, D2)
+
+
+def test_repitch_odd_k_never_reads_row_padding(tg, oracle):
+    # K = 1003 of a 1016-element row stride (16-byte rows) with NaN in the
+    # gap; the copy takes exactly K elements per row.
+    torch = torch_cuda()
+    rng = np.random.default_rng(181)
+    M, N, K, ld = 2600, 2600, 1003, 1016
+    assert tg.gemm_repitch(M, N, K, ld, ld) == 3
+    A = np.full((M, ld), 0x7FC0, np.uint16)
+    B = np.full((N, ld), 0x7FC0, np.uint16)
+    A[:, :K] = synth.bf16_uniform(rng, (M, K))
+    B[:, :K] = synth.bf16_uniform(rng, (N, K))
+    D = torch.full((M, N), float("nan"), device="cuda")
+    tg.gemm_bf16(dev_bf16(A)[:, :K], dev_bf16(B)[:, :K], D)
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    got = host_values(D)
+    rows = sample_indices(M, 64, 21, 128)
+    ref, mag = oracle.gemm_bf16(A[:, :K], B[:, :K], rows=rows)
+    assert_within(got[rows], ref, mag, False, "re-pitched odd K rows")
+    cols = sample_indices(N, 64, 22, 256)
+    ref, mag = oracle.gemm_bf16(A[:, :K], B[:, :K], cols=cols)
+    assert_within(got[:, cols], ref, mag, False, "re-pitched odd K cols")
+
+
+def test_block_scaled_calls_on_two_streams(tg, oracle):
+    # Two MXFP8 products of different shapes issued on two streams with no
+    # ordering between them: each stream has its own scale-image workspace.
+    torch = torch_cuda()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    xs = [synth.make_inputs("mx8k", M=1024, N=768, K=1024, seed=191),
+          synth.make_inputs("mx8k", M=640, N=1024, K=2048, seed=192)]
+    ins = [[dev_u8(x[k]) for k in ("A", "B", "SFA", "SFB")] for x in xs]
+    Ds = [torch.full((1024, 768), float("nan"), device="cuda"),
+          torch.full((640, 1024), float("nan"), device="cuda")]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for s, g, D in zip((s1, s2), ins, Ds):
+            with torch.cuda.stream(s):
+                tg.gemm_mxfp8_blockscaled(*g, D, stream=s)
+    torch.cuda.synchronize()
+    assert tg.tg_device_status()[0] == tg.TG_OK
+    for x, D in zip(xs, Ds):
+        ref, mag = oracle.gemm_mxfp8(x["A"], x["B"], x["SFA"], x["SFB"])
+        assert_within(host_values(D), ref, mag, False, "two streams")
 
 
 def _sampled(tg, oracle, name, out, pair, tile_m):
