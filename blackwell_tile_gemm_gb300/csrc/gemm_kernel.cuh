@@ -470,6 +470,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if constexpr (C::kCtaGroup == 2) cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch: everything above is on-chip, so it may
+  // overlap the end of the kernel before this one in the stream; operands,
+  // D and the scratch are touched only once that kernel has completed and
+  // its writes are visible.
+  griddep_wait();
 
   const WaitGuard guard{p.status, abort_flag, p.timeout_ns};
   // Work units: tiles of kPairs x 256 rows (one per cluster) by BN columns.
@@ -563,6 +568,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
       }
+      // Every load of this CTA is issued: the next kernel in the stream may
+      // start its prologue on SMs this grid frees.
+      if (warp == 0 && lane == 0) griddep_launch_dependents();
       if (!ok && leader && lane == 0) {
         for (int s = 0; s < C::kStages; ++s)
           if (issued & (1u << s))
@@ -642,6 +650,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
       }
+      // Every load of this CTA is issued: the next kernel in the stream may
+      // start its prologue on SMs this grid frees.
+      griddep_launch_dependents();
       if (!ok && leader) {
         // Gave up: let the loads already issued land before the CTA exits.
         for (int s = 0; s < C::kStages; ++s)

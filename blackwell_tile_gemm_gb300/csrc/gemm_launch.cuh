@@ -117,18 +117,23 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
     if (rc != TG_OK) return rc;
   }
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(static_cast<unsigned>(units * C::kClusterCtas), 1, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
+  // Programmatic dependent launch: the kernel's prologue may overlap the
+  // previous kernel of the stream (the kernel waits before touching memory).
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if constexpr (C::kCtaGroup == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C::kClusterCtas;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C::kClusterCtas;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<C>, tA, tB, tSFA, tSFB, tD, a);
   if (e != cudaSuccess) return cuda_fail(e);
