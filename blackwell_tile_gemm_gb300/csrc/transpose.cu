@@ -65,6 +65,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefetch_tensormap(&tm_out);
   }
   __syncthreads();
+  // Programmatic dependent launch: the set-up above may overlap the end of
+  // the previous kernel in the stream; global memory is touched only after
+  // it has completed and its writes are visible.
+  griddep_wait();
   const WaitGuard guard{status, abort_flag, timeout_ns};
   const uint64_t pol = policy_evict_first();
 
@@ -80,8 +84,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       num_tiles > static_cast<int>(blockIdx.x)
           ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
           : 0;
-  if (tid == 0)
+  if (tid == 0) {
     for (int i = 0; i < kStages && i < my_tiles; ++i) issue_load(i, i);
+    // This CTA's last load is issued: the next kernel may launch.
+    if (my_tiles <= kStages) griddep_launch_dependents();
+  }
 
   const int w = tid >> 5, lane = tid & 31;
   const int m = lane >> 3, rr = lane & 7;
@@ -135,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         bulk_commit_group();
       }
       if (i + kStages < my_tiles) issue_load(i + kStages, s);
+      if (i + kStages == my_tiles - 1) griddep_launch_dependents();
     }
   }
   if (tid == 0) {
@@ -174,11 +182,21 @@ int launch_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_ou
   const int64_t tiles = tiles_r * tiles_c;
   int64_t grid = 2 * static_cast<int64_t>(ctx->num_sms);
   if (grid > tiles) grid = tiles;
-  transpose_b16_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
-      tm_in, tm_out, static_cast<uint16_t*>(out), ld_out, static_cast<int>(rows),
-      static_cast<int>(cols), static_cast<int>(tiles_r), static_cast<int>(tiles_c), ctx->status,
-      wait_timeout_ns());
-  cudaError_t e = cudaGetLastError();
+  // Programmatic dependent launch (the kernel waits before touching memory).
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, transpose_b16_kernel, tm_in, tm_out,
+                                     static_cast<uint16_t*>(out), ld_out, static_cast<int>(rows),
+                                     static_cast<int>(cols), static_cast<int>(tiles_r),
+                                     static_cast<int>(tiles_c), ctx->status, wait_timeout_ns());
   return e == cudaSuccess ? TG_OK : cuda_fail(e);
 }
 
