@@ -11,6 +11,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <unordered_map>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -88,9 +89,52 @@ DeviceCtx* current_ctx() {
   return &c;
 }
 
+namespace {
+// Encoded maps by their complete input: an encoding is a pure function of
+// these fields, so a hit returns exactly what a fresh encode would.  Bounded
+// (cleared when full); keeps repeated calls on the same buffers off the
+// driver's encoder.
+struct MapKey {
+  uint64_t base, inner, outer, row_bytes;
+  uint32_t dtype, box_inner, box_outer, swizzle;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && row_bytes == o.row_bytes &&
+           dtype == o.dtype && box_inner == o.box_inner && box_outer == o.box_outer &&
+           swizzle == o.swizzle;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = 1469598103934665603ull;
+    const uint64_t v[8] = {k.base, k.inner, k.outer, k.row_bytes, k.dtype, k.box_inner,
+                           k.box_outer, k.swizzle};
+    for (uint64_t x : v) h = (h ^ x) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+constexpr size_t kMapCacheMax = 1024;
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+}  // namespace
+
 int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                        uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                        uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  // A zero extent is not encodable; callers never launch for empty problems,
+  // but keep a valid map (extent 1) for unused descriptor parameters.
+  if (inner == 0) inner = 1;
+  if (outer == 0) outer = 1;
+  const MapKey key{reinterpret_cast<uint64_t>(base), inner, outer, row_bytes,
+                   static_cast<uint32_t>(dtype), box_inner, box_outer,
+                   static_cast<uint32_t>(swizzle)};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mutex);
+    auto it = g_map_cache.find(key);
+    if (it != g_map_cache.end()) {
+      *map = it->second;
+      return TG_OK;
+    }
+  }
   {
     std::lock_guard<std::mutex> lk(g_mutex);
     if (g_encode == nullptr) {
@@ -104,10 +148,6 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
   }
-  // A zero extent is not encodable; callers never launch for empty problems,
-  // but keep a valid map (extent 1) for unused descriptor parameters.
-  if (inner == 0) inner = 1;
-  if (outer == 0) outer = 1;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
@@ -116,6 +156,9 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  std::lock_guard<std::mutex> lk(g_map_mutex);
+  if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+  g_map_cache.emplace(key, *map);
   return TG_OK;
 }
 
