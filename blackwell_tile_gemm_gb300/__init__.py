@@ -164,8 +164,6 @@ def _d_code(dtype):
 
 
 def _flags(cta_pair, multicast):
-    if multicast and not cta_pair:
-        raise ValueError("multicast needs cta_pair=True")
     return (TG_FLAG_CTA_PAIR if cta_pair else 0) | (TG_FLAG_MULTICAST if multicast else 0)
 
 
@@ -206,7 +204,8 @@ def gemm_bf16(A, B, D=None, *, out_dtype=None, epilogue_add=None, silu_affine=No
     A, B: CUDA bfloat16 tensors with unit inner stride.  D: optional output
     (float32 or bfloat16, [M, N]); otherwise allocated with ``out_dtype``
     (default float32).  ``cta_pair`` selects the two-CTA (cta_group::2) kernel;
-    ``multicast`` (with ``cta_pair``) runs clusters of two pairs sharing B.
+    ``multicast`` runs clusters of two units (single CTAs, or pairs with
+    ``cta_pair``) on vertically adjacent tiles that share the B tile.
     Epilogue keywords: see ``make_epilogue``.
     """
     import torch

@@ -299,7 +299,6 @@ int check_gemm_common(const void* A, int64_t lda, const void* B, int64_t ldb, vo
   if (epilogue < TG_EPI_NONE || epilogue > TG_EPI_BIAS_COL_SILU) return TG_ERR_INVALID_ARG;
   if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST))
     return TG_ERR_UNSUPPORTED;
-  if ((flags & TG_FLAG_MULTICAST) && !(flags & TG_FLAG_CTA_PAIR)) return TG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TG_OK;
   if (D == nullptr || ldd < N) return TG_ERR_INVALID_ARG;
   const int d_esize = d_dtype == TG_D_F32 ? 4 : 2;
@@ -327,9 +326,9 @@ int check_blockscaled_args(int kind, const void* A, int64_t lda, const void* B, 
   if (kind != kKindMxf8 && kind != kKindMxf4 && kind != kKindNvf4) return TG_ERR_INVALID_ARG;
   const int block = scale_block_of(kind);
   if (K % block != 0) return TG_ERR_INVALID_ARG;
-  // Multicast clusters exist for MXFP8 only.
-  if (kind != kKindMxf8 && (flags & TG_FLAG_MULTICAST) && (flags & TG_FLAG_CTA_PAIR))
-    return TG_ERR_UNSUPPORTED;
+  // Block-scaled multicast clusters are made of CTA pairs, for MXFP8 only.
+  if ((flags & TG_FLAG_MULTICAST) && !(flags & TG_FLAG_CTA_PAIR)) return TG_ERR_INVALID_ARG;
+  if (kind != kKindMxf8 && (flags & TG_FLAG_MULTICAST)) return TG_ERR_UNSUPPORTED;
   int rc = check_gemm_common(A, lda, B, ldb, D, ldd, M, N, K, d_dtype, epilogue, flags, 1,
                              kind == kKindMxf8 ? 1 : 2);
   if (rc != TG_OK || M == 0 || N == 0) return rc;

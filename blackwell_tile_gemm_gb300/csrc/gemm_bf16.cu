@@ -22,19 +22,28 @@ using CfgPairBf16 = GemmCfg<2, kKindBf16, 256, 2, 6, true>;
 // Clusters of two CTA pairs multicasting the shared B tile (TG_FLAG_MULTICAST).
 using CfgPairMcF32 = GemmCfg<2, kKindBf16, 256, 2, 6, false, true>;
 using CfgPairMcBf16 = GemmCfg<2, kKindBf16, 256, 2, 6, true, true>;
+// Clusters of two single CTAs on vertically adjacent tiles multicasting the
+// shared B tile (each loads 128 of its 256 rows).
+using CfgMcF32 = GemmCfg<1, kKindBf16, 256, 2, 4, false, true>;
+using CfgMcBf16 = GemmCfg<1, kKindBf16, 256, 2, 4, true, true>;
 }  // namespace
+
+bool single_cta_multicast_pays(int64_t M, int64_t N, int64_t K) {
+  return K <= 1536 && M >= 3000 && N >= 3000;
+}
 
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
                           int64_t ldd, int M, int N, int K, int d_dtype, const Epi& epi,
                           bool pair, bool mcast, cudaStream_t stream, DeviceCtx* ctx) {
   constexpr int BN = 256;
+  if (!pair && !mcast && single_cta_multicast_pays(M, N, K)) mcast = true;
   const int g = pair ? 2 : 1;
   const int b_rows = BN / g;
   CUtensorMap tA, tB;
   int rc = make_tensor_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, lda * 2, 64, 128,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != TG_OK) return rc;
-  const int b_box = pair && mcast ? b_rows / 2 : b_rows;
+  const int b_box = mcast ? b_rows / 2 : b_rows;
   rc = make_tensor_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, ldb * 2, 64, b_box,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != TG_OK) return rc;
@@ -52,6 +61,14 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
   const bool bf16_out = d_dtype == TG_D_BF16;
+  // Single CTAs: for short K on large products, clusters of two sharing the
+  // B tile by multicast cut each CTA's loads from 48 to 32 KB a stage
+  // (graph replay: 4096^2 x 512 23.9 -> 18.4 us, 4096^2 x 1024 32.6 ->
+  // 27.8, 8192^2 x 1024 96.6 -> 90.5, 4000 x 3000 x 1000 28.6 -> 27.0); at
+  // K >= 2048 the coupled rings cost more than they save (4096^3 89 -> 95).
+  if (!pair && mcast)
+    return bf16_out ? launch_gemm_cfg<CfgMcBf16>(tA, tB, tA, tB, a, stream, ctx)
+                    : launch_gemm_cfg<CfgMcF32>(tA, tB, tA, tB, a, stream, ctx);
   if (!pair)
     return bf16_out ? launch_gemm_cfg<CfgBf16>(tA, tB, tA, tB, a, stream, ctx)
                     : launch_gemm_cfg<CfgF32>(tA, tB, tA, tB, a, stream, ctx);
@@ -63,6 +80,7 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
 }
 
 int bf16_tail_split(int64_t M, int64_t N, int64_t K, bool pair, DeviceCtx* ctx) {
+  if (!pair && single_cta_multicast_pays(M, N, K)) return 1;   // clusters never split
   const int g = pair ? 2 : 1;
   const int num_tiles = ceil_div_i(M, 128 * g) * ceil_div_i(N, 256);
   const int units_max =

@@ -173,7 +173,7 @@ struct GemmCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
-  static_assert(!kMcast || kCtaGroup == 2, "multicast clusters are made of CTA pairs");
+  static_assert(!kMcast || kCtaGroup == 2 || !kMx, "single-CTA multicast clusters: bf16 only");
   static_assert(!kMx || BN % 128 == 0, "scale images cover 128-row blocks of B");
   static_assert(!kGather || (!kMx && !kMcast), "gathered A: bf16, without multicast");
 };
@@ -423,15 +423,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
-  const uint32_t rank = (C::kCtaGroup == 2) ? cluster_ctarank() : 0u;
-  const uint32_t pair_rank = rank & 1u;               // 0: MMA-issuing CTA of the pair
-  const uint32_t pair_id = rank >> 1;                 // which pair of the cluster
-  const uint32_t lead_rank = rank & ~1u;              // rank of this pair's leader
+  // An MMA unit is a CTA pair (cta_group::2) or a single CTA; a multicast
+  // cluster holds two units on vertically adjacent tiles.
+  const uint32_t rank = (C::kClusterCtas > 1) ? cluster_ctarank() : 0u;
+  const uint32_t pair_rank = C::kCtaGroup == 2 ? (rank & 1u) : 0u;  // 0: MMA-issuing CTA
+  const uint32_t pair_id = rank / C::kCtaGroup;       // which unit of the cluster
+  const uint32_t lead_rank = rank - pair_rank;        // rank of this unit's leader
   const bool leader = pair_rank == 0;
-  // tcgen05.commit multicast masks: this pair, and every CTA whose loads
-  // land in this pair's shared memory (both pairs under multicast).
-  const uint16_t pair_mask = static_cast<uint16_t>(3u << lead_rank);
-  const uint16_t stage_mask = C::kMcast ? static_cast<uint16_t>(0xF) : pair_mask;
+  // tcgen05.commit multicast masks: this unit, and every CTA whose loads
+  // land in this unit's shared memory (the whole cluster under multicast).
+  const uint16_t pair_mask =
+      static_cast<uint16_t>((C::kCtaGroup == 2 ? 3u : 1u) << lead_rank);
+  const uint16_t stage_mask =
+      C::kMcast ? static_cast<uint16_t>((1u << C::kClusterCtas) - 1u) : pair_mask;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (C::kCtaGroup == 2) cluster_sync();
+  if constexpr (C::kClusterCtas > 1) cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // Programmatic dependent launch: everything above is on-chip, so it may
@@ -589,7 +593,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t full0 = smem_addr(&full_bar[0]);
       // Pair: both CTAs' loads complete on the leader's barrier.
       const uint32_t full_dst0 = C::kCtaGroup == 2 ? map_to_cta(full0, lead_rank) : full0;
-      const uint16_t mcast_mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2u)));
+      // The same CTA of the other unit: rank ^ kCtaGroup.
+      const uint16_t mcast_mask = static_cast<uint16_t>(
+          (1u << rank) | (1u << (rank ^ static_cast<uint32_t>(C::kCtaGroup))));
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;   // per-stage bit masks
@@ -615,7 +621,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if constexpr (C::kCtaGroup == 1) {
             mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_TX);
             tma_load_2d(sA + stage * C::A_BYTES, &tmA, fb, kx, a_row, pol_ab);
-            tma_load_2d(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+            if constexpr (C::kMcast) {
+              // This CTA's half of the B tile, into itself and the other
+              // CTA of the cluster (same offset in both).
+              tma_load_2d_mcast(sB + stage * C::B_BYTES + pair_id * (C::B_LOAD_ROWS * 128), &tmB,
+                                fb, kx, b_row + static_cast<int>(pair_id) * C::B_LOAD_ROWS,
+                                mcast_mask, pol_ab);
+            } else {
+              tma_load_2d(sB + stage * C::B_BYTES, &tmB, fb, kx, b_row, pol_ab);
+            }
             if constexpr (C::kMx) {
               tma_load_2d(sSFA + stage * C::SFA_BYTES, &tmSFA, fb, 0, kb * p.sfa_blocks + sfa_row,
                           pol_ab);
@@ -722,7 +736,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           }
-          if constexpr (C::kCtaGroup == 1)
+          if constexpr (C::kCtaGroup == 1 && C::kMcast)
+            mma_commit_mc(&empty_bar[stage], stage_mask);
+          else if constexpr (C::kCtaGroup == 1)
             mma_commit(&empty_bar[stage]);
           else
             mma_commit_pair(&empty_bar[stage], stage_mask);
@@ -1058,7 +1074,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (C::kCtaGroup == 2) cluster_sync();
+  if constexpr (C::kClusterCtas > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc<C::kCtaGroup>(tmem_base, C::TMEM_COLS);

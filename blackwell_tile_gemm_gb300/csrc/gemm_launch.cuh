@@ -29,7 +29,7 @@ int gemm_units_for_device(DeviceCtx* ctx) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return -cuda_fail(e);
   int units = ctx->num_sms / C::kClusterCtas;
-  if constexpr (C::kCtaGroup == 2) {
+  if constexpr (C::kClusterCtas > 1) {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -128,7 +128,7 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if constexpr (C::kCtaGroup == 2) {
+  if constexpr (C::kClusterCtas > 1) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = C::kClusterCtas;
     attr[1].val.clusterDim.y = 1;

@@ -285,6 +285,19 @@ __device__ __forceinline__ void tma_load_2d_pair_mcast(uint32_t dst, const CUten
       : "memory");
 }
 
+// Single-CTA multicast load: the box lands at offset `dst` of every CTA in
+// `cta_mask` and completes bytes on the barrier at offset `bar` of each.
+__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const CUtensorMap* map,
+                                                  uint32_t bar, int32_t x, int32_t y,
+                                                  uint16_t cta_mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask),
+      "l"(policy)
+      : "memory");
+}
+
 // Row gather ("cp.async.bulk.tensor", section "Gather4 and scatter4"): four
 // rows r0..r3 of a 2-D map whose box is one row high, columns x .. x+width,
 // into four consecutive box images at dst, completing on `bar`.  Rows
@@ -615,6 +628,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_addr(bar))
+      : "memory");
+}
+
+// Single-CTA MMAs, arriving on the barrier at the same offset in every CTA
+// of `cta_mask` (clusters whose CTAs share staged operands).
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 

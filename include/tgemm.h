@@ -108,11 +108,16 @@ typedef struct tg_epilogue {
 enum {
   TG_FLAG_CTA_PAIR = 1u, /* cta_group::2: two CTAs of a cluster share one
                             256-row MMA; each loads half of the B tile      */
-  TG_FLAG_MULTICAST = 2u, /* with TG_FLAG_CTA_PAIR only: clusters of two pairs
-                            on vertically adjacent tiles share the B tile by
-                            TMA multicast (each CTA loads a quarter).  Same
-                            results; on GB300 measured 2-3% slower than plain
-                            pairs at 8192^3, so it is off by default.       */
+  TG_FLAG_MULTICAST = 2u, /* clusters of two MMA units on vertically adjacent
+                            tiles share the B tile by TMA multicast.  With
+                            TG_FLAG_CTA_PAIR: two pairs (each CTA loads a
+                            quarter of B); measured 2-3% slower than plain
+                            pairs at 8192^3, so off by default.  Alone (bf16
+                            only): two single CTAs, each loading half of B;
+                            gemm_bf16 with flags 0 picks these by itself for
+                            K <= 1536 with M, N >= 3000, where they measured
+                            6-30% faster (slower at K >= 2048).  Same
+                            results either way.                              */
   TG_FLAG_GATHER_TMA = 4u /* gemm_bf16_gather only: load the gathered A rows
                             inside the GEMM with TMA tile::gather4 instead
                             of copying them into the workspace first.  Same
@@ -130,8 +135,8 @@ enum {
  *          loads past the edge read zeros [TMA], stores past it are dropped.
  *   epilogue, epi_scalar: TG_EPI_NONE, or TG_EPI_ADD_SCALAR with constant s
  *          (the other epilogues need gemm_bf16_ex).
- *   flags: 0, TG_FLAG_CTA_PAIR, or TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST
- *          (TG_FLAG_MULTICAST alone: TG_ERR_INVALID_ARG).
+ *   flags: 0, TG_FLAG_CTA_PAIR, TG_FLAG_MULTICAST (single-CTA clusters), or
+ *          TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST.
  * Rounding: f32 -> bf16 D is round-to-nearest-even.  Alignment: A, B, D
  * 16-byte aligned; lda*2, ldb*2, ldd*sizeof(D) multiples of 16.
  * Re-pitch: when lda*2 (or ldb*2) is not a multiple of 32 (rows only 16-byte
@@ -163,7 +168,8 @@ int gemm_bf16_ex(const void* A, int64_t lda, const void* B, int64_t ldb, void* D
  *   B   : device, FP8 E4M3FN bytes [N, K], row stride ldb.
  *   SFA : device, E8M0 bytes [M, K/32], row stride ld_sfa (any value >= K/32).
  *   SFB : device, E8M0 bytes [N, K/32], row stride ld_sfb.
- *   D, ldd, d_dtype, epilogue, epi_scalar, flags: as for gemm_bf16.
+ *   D, ldd, d_dtype, epilogue, epi_scalar, flags: as for gemm_bf16, except
+ *   that TG_FLAG_MULTICAST needs TG_FLAG_CTA_PAIR (alone: TG_ERR_INVALID_ARG).
  *   K must be a multiple of 32 (one scale per 32 K elements); otherwise
  *   TG_ERR_INVALID_ARG.  lda and ldb must be multiples of 16.
  * The scales are first rearranged on the device into the tensor-memory image
@@ -251,7 +257,8 @@ int tg_skinny_split_count(int64_t N, int64_t K, int split_k);
  *   B   : device, packed E2M1 [N, K/2] bytes, row stride ldb (bytes).
  *   SFA : device, E8M0 bytes [M, K/32], row stride ld_sfa (>= K/32).
  *   SFB : device, E8M0 bytes [N, K/32], row stride ld_sfb.
- *   D, ldd, d_dtype, epi, flags: as for gemm_bf16_ex.
+ *   D, ldd, d_dtype, epi: as for gemm_bf16_ex.  flags: 0 or TG_FLAG_CTA_PAIR
+ *   (TG_FLAG_MULTICAST: TG_ERR_UNSUPPORTED with a pair, else TG_ERR_INVALID_ARG).
  *   K must be a multiple of 32; otherwise TG_ERR_INVALID_ARG.  lda >= K/2,
  *   ldb >= K/2, both multiples of 16 (TG_ERR_MISALIGNED).
  * The scales are rearranged into the tensor-memory image in the stream's

@@ -58,7 +58,6 @@ A16 = 0x10000           # a 16-byte aligned fake device address (never dereferen
     (dict(d_dtype=7), tg.TG_ERR_INVALID_ARG),
     (dict(epilogue=9), tg.TG_ERR_INVALID_ARG),
     (dict(flags=0x80), tg.TG_ERR_UNSUPPORTED),
-    (dict(flags=2), tg.TG_ERR_INVALID_ARG),         # multicast without CTA pairs
     (dict(A=0), tg.TG_ERR_INVALID_ARG),
     (dict(D=0), tg.TG_ERR_INVALID_ARG),
     (dict(lda=32), tg.TG_ERR_INVALID_ARG),          # lda < K
@@ -92,6 +91,8 @@ def test_mxfp8_rejects_bad_k_and_scales(L):
     assert f(A16, 64, A16, 64, A16, 1, A16, 2, A16, 64, 64, 64, 64, 0, 0, 0.0, 0, None) == 1
     # lda = 40 bytes is not a multiple of 16
     assert f(A16, 40, A16, 64, A16, 2, A16, 2, A16, 64, 64, 64, 32, 0, 0, 0.0, 0, None) == 2
+    # block-scaled multicast clusters are made of CTA pairs
+    assert f(A16, 64, A16, 64, A16, 2, A16, 2, A16, 64, 64, 64, 64, 0, 0, 0.0, 2, None) == 1
 
 
 def test_transpose_rejects_bad_arguments(L):
@@ -145,6 +146,7 @@ def test_fp4_rejects_before_launch(L, fn, block):
     assert call(ls=128 // block - 1) == tg.TG_ERR_INVALID_ARG          # ld_sfa < K/block
     assert call(SFB=0) == tg.TG_ERR_INVALID_ARG
     assert call(flags=3) == tg.TG_ERR_UNSUPPORTED                     # no FP4 multicast
+    assert call(flags=2) == tg.TG_ERR_INVALID_ARG                     # multicast needs pairs
     assert call(M=0) == tg.TG_OK
 
 

@@ -46,7 +46,7 @@ def _check(oracle, got, ref, mag, op, bias_np, lip, bf16_out, what):
 
 @pytest.mark.parametrize("name,op,kw,lip", CASES, ids=[c[0] for c in CASES])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-@pytest.mark.parametrize("pair", [False, True, "mc"])
+@pytest.mark.parametrize("pair", [False, True, "mc", "mc1"])
 def test_bf16_gemm_epilogues(tg, oracle, name, op, kw, lip, out, pair):
     torch = torch_cuda()
     rng = np.random.default_rng(op * 10 + (out == "bf16"))
@@ -56,8 +56,8 @@ def test_bf16_gemm_epilogues(tg, oracle, name, op, kw, lip, out, pair):
     bias = torch.from_numpy(bias_np).cuda()
     dt = torch.float32 if out == "f32" else torch.bfloat16
     D = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
-    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), D, cta_pair=bool(pair), multicast=pair == "mc",
-                 **kw(bias))
+    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), D, cta_pair=pair in (True, "mc"),
+                 multicast=pair in ("mc", "mc1"), **kw(bias))
     assert tg.tg_device_status()[0] == tg.TG_OK
     ref, mag = oracle.gemm_bf16(A, B)
     _check(oracle, host_values(D), ref, mag, op, bias_np, lip(), out == "bf16", name)

@@ -25,7 +25,7 @@ def tg():
 
 
 # `pair`: False = single CTA, True = CTA pair, "mc" = clusters of two pairs
-# sharing the B tile by multicast.
+# sharing the B tile by multicast, "mc1" = clusters of two single CTAs sharing it.
 def run_bf16(tg, A, B, out_dtype="f32", add=None, pair=False, ld_pad=0):
     torch = torch_cuda()
     M, K = A.shape
@@ -36,8 +36,8 @@ def run_bf16(tg, A, B, out_dtype="f32", add=None, pair=False, ld_pad=0):
         D = Dfull[:, :N]
     else:
         D = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
-    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), D, epilogue_add=add, cta_pair=bool(pair),
-                 multicast=pair == "mc")
+    tg.gemm_bf16(dev_bf16(A), dev_bf16(B), D, epilogue_add=add, cta_pair=pair in (True, "mc"),
+                 multicast=pair in ("mc", "mc1"))
     assert tg.tg_device_status()[0] == tg.TG_OK
     return D
 
@@ -58,7 +58,7 @@ def quarter_bits(rng, shape):
 
 # ------------------------------------------------------------------ bf16, small
 
-@pytest.mark.parametrize("pair", [False, True, "mc"])
+@pytest.mark.parametrize("pair", [False, True, "mc", "mc1"])
 def test_tiny_workload_full(tg, oracle, pair):
     x = synth.make_inputs("tiny")
     D = run_bf16(tg, x["A"], x["B"], "f32", pair=pair)
@@ -66,7 +66,7 @@ def test_tiny_workload_full(tg, oracle, pair):
     assert_within(host_values(D), ref, mag, False, "tiny")
 
 
-@pytest.mark.parametrize("pair", [False, True, "mc"])
+@pytest.mark.parametrize("pair", [False, True, "mc", "mc1"])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 512), (384, 256, 1024), (128, 256, 64)])
 def test_quarter_integers_bit_exact(tg, oracle, pair, M, N, K):
     rng = np.random.default_rng(M + N + K)
@@ -76,7 +76,7 @@ def test_quarter_integers_bit_exact(tg, oracle, pair, M, N, K):
     assert np.array_equal(host_values(D), ref)
 
 
-@pytest.mark.parametrize("pair", [False, True, "mc"])
+@pytest.mark.parametrize("pair", [False, True, "mc", "mc1"])
 def test_one_hot_across_tile_edges(tg, pair):
     M, N, K = 512, 512, 192
     one = 0x3F80
@@ -102,7 +102,7 @@ def test_identity(tg):
     assert np.array_equal(got, synth.bf16_bits_to_f32(A).astype(np.float64))
 
 
-@pytest.mark.parametrize("pair", [False, True, "mc"])
+@pytest.mark.parametrize("pair", [False, True, "mc", "mc1"])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N,K", [(1, 8, 16), (33, 40, 40), (130, 264, 72), (300, 520, 1000),
                                    (129, 8, 8)])
@@ -311,7 +311,7 @@ def test_mx8k_workload_sampled(tg, oracle):
 
 # ------------------------------------------------------- outside D, outside K
 
-@pytest.mark.parametrize("pair", [False, True, "mc"])
+@pytest.mark.parametrize("pair", [False, True, "mc", "mc1"])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N,K", [(1, 1, 64), (37, 13, 72), (129, 250, 64), (260, 300, 200),
                                    (300, 67, 128), (128, 192, 64)])
@@ -326,7 +326,7 @@ def test_d_window_leaves_surroundings(tg, oracle, pair, out, M, N, K):
     ldd = (N + 1 + 7) // 8 * 8
     Dfull = torch.full((M + 40, ldd), float("nan"), dtype=dt, device="cuda")
     tg.gemm_bf16(dev_bf16(A), dev_bf16(B), Dfull[:M, :N], epilogue_add=1.0,
-                 cta_pair=bool(pair), multicast=pair == "mc")
+                 cta_pair=pair in (True, "mc"), multicast=pair in ("mc", "mc1"))
     assert tg.tg_device_status()[0] == tg.TG_OK
     got = host_values(Dfull)
     ref, mag = oracle.gemm_bf16(A, B, add=1.0)
