@@ -458,6 +458,34 @@ def run_configs(args):
             times.append(e0.elapsed_time(e1) / 10)
         return statistics.median(times)
 
+    side = torch.cuda.Stream()
+
+    def graph_ms(fn):
+        # device time per call without host overhead: a CUDA graph of 10
+        # calls captured on a side stream (warmed up there first, so that its
+        # workspace exists before capture), median of 5 replays
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(10):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(5):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(side)
+                g.replay()
+                e1.record(side)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) / 10)
+        del g
+        return statistics.median(times)
+
     # Fused-epilogue rows: the same 8192^3 products with each non-trivial op.
     bias = torch.linspace(-2.0, 2.0, SIZE, device=dev, dtype=torch.float32)
     epilogue_rows = {"silu_affine": dict(silu_affine=(1.5, -0.25)), "bias": dict(bias=bias),
@@ -503,32 +531,38 @@ def run_configs(args):
             else:
                 fn = lambda: tg.gemm_bf16(A, B, D, cta_pair=w.cta_pair, **epi)  # noqa: E731
         ms = median_ms(fn)
+        ms_g = graph_ms(fn)
         code, _ = tg.tg_device_status()
         line = {"workload": name, "describe": w.describe, "status": code, "ms_median": ms,
-                "timing": "median of 5 rounds of 10 back-to-back calls"}
+                "timing": "median of 5 rounds of 10 back-to-back calls",
+                "ms_graph": ms_g,
+                "timing_graph": "CUDA graph of 10 calls, median of 5 replays (no host overhead)"}
         if epi:
             line["epilogue"] = sorted(epi)
         if w.kind == "transpose":
             gbs = 2 * 2 * w.M * w.N / (ms * 1e-3) / 1e9
-            line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]))
+            line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]),
+                        gbs_graph=2 * 2 * w.M * w.N / (ms_g * 1e-3) / 1e9)
         elif w.kind == "skinny":
             # algorithmic bytes: B and A read once, D written once (bf16)
             nbytes = 2 * w.N * w.K + 2 * w.M * w.K + 2 * w.M * w.N
             gbs = nbytes / (ms * 1e-3) / 1e9
             line.update(gbs=gbs, frac_of_hbm=gbs / float(peaks["hbm_gbs"]),
+                        gbs_graph=nbytes / (ms_g * 1e-3) / 1e9,
                         tflops=w.flops / (ms * 1e-3) / 1e12,
                         splits=tg.skinny_split_count(w.N, w.K, 0),
                         tile_kernel_ms=ms_tile)
         elif w.kind == "gather":
             tf = w.flops / (ms * 1e-3) / 1e12
             line.update(tflops=tf, frac_of_cublas_bf16_burst_scaled=tf / float(peaks["bf16_tflops"]),
-                        dense_same_shape_ms=ms_tile)
+                        tflops_graph=w.flops / (ms_g * 1e-3) / 1e12, dense_same_shape_ms=ms_tile)
         else:
             tf = w.flops / (ms * 1e-3) / 1e12
             # nominal dense ratios to bf16 (2.25 / 4.5 / 13.5 PFLOP/s per GPU)
             ratio = {"mxfp8": 2, "mxfp4": 6, "nvfp4": 6}.get(w.kind, 1)
             pk = float(peaks["bf16_tflops"]) * ratio
-            line.update(tflops=tf, frac_of_cublas_bf16_burst_scaled=tf / pk)
+            line.update(tflops=tf, frac_of_cublas_bf16_burst_scaled=tf / pk,
+                        tflops_graph=w.flops / (ms_g * 1e-3) / 1e12)
             if w.kind in ("mxfp4", "nvfp4"):
                 # the tensor-pipe rate the FP4 rate probe measures: 4x bf16 per clock
                 line["frac_of_probe_rate_4x_bf16"] = tf / (float(peaks["bf16_tflops"]) * 4)
