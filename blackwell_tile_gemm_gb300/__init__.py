@@ -51,6 +51,10 @@ class tg_epilogue(ctypes.Structure):
                 ("bias", ctypes.c_void_p)]
 
 
+# The no-op epilogue, shared (the C calls only read it).
+_EPI_NONE = tg_epilogue(0, 0.0, 0.0, None)
+
+
 class TgError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
@@ -64,6 +68,9 @@ class TgError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """The loaded libtgemm.so (raises if it has not been built)."""
     global _lib
+    L = _lib
+    if L is not None:
+        return L
     with _lock:
         if _lib is not None:
             return _lib
@@ -127,6 +134,9 @@ def status_string(code: int) -> str:
 def _stream_handle(stream):
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:       # the current stream's handle without a Stream object
+            return ctypes.c_void_p(raw(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     if isinstance(stream, int):
         return ctypes.c_void_p(stream)
@@ -139,11 +149,14 @@ def _check(rc: int, what: str) -> None:
 
 
 def _rows(t, name):
-    if t.dim() != 2:
+    shape = t.shape
+    if len(shape) != 2:
         raise ValueError(f"{name} must be 2-D")
-    if t.shape[0] > 0 and t.shape[1] > 0 and t.stride(1) != 1:
+    rows, cols = shape
+    st = t.stride()
+    if rows > 0 and cols > 0 and st[1] != 1:
         raise ValueError(f"{name} must have unit inner stride")
-    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+    return st[0] if rows > 1 else max(cols, 1)
 
 
 def _ld(t, name, mult):
@@ -176,6 +189,8 @@ def make_epilogue(epilogue_add=None, silu_affine=None, bias=None, bias_silu=Fals
     bias=<f32 CUDA tensor [N]>: D = acc + bias[j], or with bias_silu=True
     D = silu(acc + bias[j]).
     """
+    if epilogue_add is None and silu_affine is None and bias is None and affine is None:
+        return _EPI_NONE
     chosen = [epilogue_add is not None, silu_affine is not None, bias is not None,
               affine is not None]
     if sum(chosen) > 1:
