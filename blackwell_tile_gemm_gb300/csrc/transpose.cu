@@ -19,6 +19,7 @@
 //      into the output tile at block (8c, 8w), same swizzle;
 //   3. one thread TMA-stores the output tile (edge tiles: element-wise stores
 //      inside the array) and refills stage s.
+#include <atomic>
 #include <cstdint>
 
 #include <cuda.h>
@@ -172,12 +173,14 @@ int launch_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_ou
                           static_cast<uint64_t>(ld_out) * 2, kTile, kTile,
                           CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != TG_OK) return rc;
-  static bool attr_set[64] = {};
-  if (!attr_set[ctx->device]) {
+  // Once per device (setting it twice is harmless; the flag is atomic so
+  // that concurrent first calls do not race on it).
+  static std::atomic<bool> attr_set[64];
+  if (!attr_set[ctx->device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(transpose_b16_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
-    attr_set[ctx->device] = true;
+    attr_set[ctx->device].store(true, std::memory_order_release);
   }
   const int64_t tiles = tiles_r * tiles_c;
   int64_t grid = 2 * static_cast<int64_t>(ctx->num_sms);

@@ -26,7 +26,9 @@
  *     that needs it, grown on demand (growing synchronises that stream, so
  *     make the largest call on a stream before capturing it into a graph),
  *     never shrunk, freed at process exit.  Calls on different streams never
- *     share workspace.  The transpose allocates nothing.
+ *     share workspace.  The transpose allocates nothing.  A CUDA graph
+ *     captured from a stream keeps that stream's workspace addresses: do not
+ *     replay it concurrently with itself or with other work on that stream.
  *   - Strides are in ELEMENTS and describe row-major 2-D arrays (unit inner
  *     stride).  Pointers are device pointers and must be 16-byte aligned;
  *     every row stride times the element size must be a multiple of 16 bytes.
