@@ -18,18 +18,27 @@
 //               of 32 bytes of K each, and commits to the slot's "empty"
 //               barrier; at the end of a tile it commits to the accumulator's
 //               "full" barrier.
-//   warps 2..9  epilogue: wait for a full accumulator; each warp reads its
-//               32 TMEM lanes x BN/2 columns with tcgen05.ld (row = lane) into
-//               registers and releases the accumulator at once, then applies
-//               the scalar op, converts and stores with st.global.v4.
+//   warps 2..9  epilogue: wait for a full accumulator; each warp owns 32
+//               TMEM lanes (rows) x BN/2 columns.  With two accumulators it
+//               reads one 32-row x 128-byte box at a time (tcgen05.ld,
+//               row = lane), applies the fused op, converts, stages the box
+//               128B-swizzled in shared memory and stores it with a TMA tile
+//               store, handing the accumulator back after its last read.
+//               With one accumulator (block-scaled kinds) it reads its whole
+//               share at once, hands the accumulator back, then stores from
+//               registers with st.global.v4 (also used for boxes that cross
+//               column N).
 //   warps 10,11 block-scaled kinds only: scale copiers; once a stage's data
 //               has landed, each copies half of its scale images into the
 //               stage's TMEM scale columns (tcgen05.cp) and commits to the
 //               stage's "scales ready" barrier, which the MMAs wait for.
 //
-// Tiles are visited persistently (one CTA or CTA pair per SM, static stride)
-// in grouped order so that CTAs running at the same time share A and B panels
-// in L2.  Every wait is bounded (see tg_ptx.cuh: mbar_wait).
+// Tiles are visited persistently (one MMA unit -- a CTA, or a CTA pair --
+// per SM or SM pair, static stride) in grouped order so that units running at
+// the same time share A and B panels in L2; multicast clusters pair two units
+// on vertically adjacent tiles that share the B tile; the last wave's tiles
+// may be cut into K pieces (tail split, see next_work).  Every wait is
+// bounded (see tg_ptx.cuh: mbar_wait).
 #pragma once
 
 #include <cstdint>
