@@ -25,9 +25,10 @@
 //               128B-swizzled in shared memory and stores it with a TMA tile
 //               store, handing the accumulator back after its last read.
 //               With one accumulator (block-scaled kinds) it reads its whole
-//               share at once, hands the accumulator back, then stores from
-//               registers with st.global.v4 (also used for boxes that cross
-//               column N).
+//               share at once and hands the accumulator back, then stores
+//               each chunk through 32-row x 64-byte staged boxes with TMA
+//               (where shared memory allows; else, and for chunks that cross
+//               column N, from registers with st.global.v4).
 //   warps 10,11 block-scaled kinds only: scale copiers; once a stage's data
 //               has landed, each copies half of its scale images into the
 //               stage's TMEM scale columns (tcgen05.cp) and commits to the
@@ -139,17 +140,24 @@ struct GemmCfg {
   static constexpr int kSfWarps = kMx ? 2 : 0;
   static constexpr int NUM_BARS =
       (kMx ? 3 : 2) * kStages + 2 * kAccBufs + 1 + kSfWarps;
-  // TMA-store epilogue, with two accumulator buffers and where shared
-  // memory allows: each epilogue warp stages 32 rows x 128 bytes (32 f32 or
-  // 64 bf16 columns) at a time, 128B swizzled, and one lane stores the box
-  // with TMA (full 128-byte lines).  The block-scaled rings (one accumulator,
-  // which their epilogue must hand back as early as possible) store from
-  // registers with st.global.v4.
+  // TMA-store epilogue, where shared memory allows: each epilogue warp
+  // stages one box of 32 rows at a time and one lane stores it with TMA.
+  // With two accumulators the boxes are 128 bytes wide (32 f32 or 64 bf16
+  // columns, 128B swizzle) and are read from TMEM box by box; the
+  // block-scaled rings (one accumulator, which their epilogue must hand back
+  // as early as possible) read everything first and stage 64-byte boxes
+  // (64B swizzle), whose 2 KB per warp fit beside the MXFP8 ring.  Without
+  // room (the MXFP4 pair ring) the warps store from registers with
+  // st.global.v4.
   static constexpr int OFF_SF_END = OFF_SFB + kStages * SFB_BYTES;
-  static constexpr int kStgWarpBytes = 32 * 128;
+  // Staged box rows: 128 bytes with two accumulators (box-wise epilogue),
+  // 64 bytes with one (the whole share is read first; 2 KB per warp fits
+  // beside the block-scaled rings).
+  static constexpr int kStgRowBytes = kAccBufs == 2 ? 128 : 64;
+  static constexpr int kStgWarpBytes = 32 * kStgRowBytes;
   static constexpr int OFF_STG = (OFF_SF_END + 1023) & ~1023;
   static constexpr bool kTmaStore =
-      kAccBufs == 2 && OFF_STG + 8 * kStgWarpBytes + NUM_BARS * 8 + 16 + 1024 <= 227 * 1024;
+      OFF_STG + 8 * kStgWarpBytes + NUM_BARS * 8 + 16 + 1024 <= 227 * 1024;
   static constexpr int OFF_BAR = kTmaStore ? OFF_STG + 8 * kStgWarpBytes : ((OFF_SF_END + 7) & ~7);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -401,6 +409,30 @@ __device__ __forceinline__ void epilogue_stage_box(uint32_t stg_row, uint32_t la
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         w[e] = kAdd ? __float_as_uint(__uint_as_float(va[4 * j + e]) + add) : va[4 * j + e];
+    }
+    st_shared_v4(stg_row + ((static_cast<uint32_t>(j) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+  }
+}
+
+// One 32-row x 64-byte box (lane = row) of chunk v into the warp's staging
+// buffer, 64B-swizzled: 16-byte piece j of row r at r*64 + ((j ^ ((r >> 1) &
+// 3)) * 16).  bf16: the chunk's 32 columns; f32: columns 16h .. 16h+15.
+template <class C>
+__device__ __forceinline__ void epilogue_stage_box64(uint32_t stg_row, uint32_t lane,
+                                                     const uint32_t (&v)[32], int h, float add) {
+  const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w[4];
+    if constexpr (C::kBf16Out) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(v[8 * j + 2 * e]) + add,
+                           __uint_as_float(v[8 * j + 2 * e + 1]) + add);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = __float_as_uint(__uint_as_float(v[16 * h + 4 * j + e]) + add);
     }
     st_shared_v4(stg_row + ((static_cast<uint32_t>(j) ^ sw) << 4), w[0], w[1], w[2], w[3]);
   }
@@ -833,7 +865,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // This warp's staging buffer for the TMA-store epilogue.
     const uint32_t stg =
         smem_addr(smem + C::OFF_STG) + static_cast<uint32_t>(warp - 2) * C::kStgWarpBytes;
-    const uint32_t stg_row = stg + lane * 128u;
+    const uint32_t stg_row = stg + lane * static_cast<uint32_t>(C::kStgRowBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t acce_remote = 0;
@@ -866,7 +898,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         return p.flags + (static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup +
                pair_rank;
       };
-      if constexpr (C::kTmaStore) {
+      if constexpr (C::kTmaStore && C::kAccBufs == 2) {
         // Box-wise: the accumulator is read one box (32 rows x 128 bytes of
         // D) at a time, which keeps 32 or 64 values live instead of 128; the
         // second accumulator buffer lets the MMA warp run ahead meanwhile.
@@ -1051,7 +1083,38 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
         const int col_base = tn * C::BN + half * C::kEpiCols;
-        if (epi_lean) {
+        if constexpr (C::kTmaStore) {
+          // One accumulator, staged stores: boxes of 32 rows x 64 bytes (32
+          // bf16 or 16 f32 columns), 64B-swizzled; a chunk crossing column N
+          // is stored from registers.
+          const int row0 = row - static_cast<int>(lane);
+          constexpr int kBoxCols = C::kStgRowBytes / (C::kBf16Out ? 2 : 4);
+          constexpr int kBoxes = 32 / kBoxCols;
+          const float add = epi_lean ? epi_add : 0.0f;
+#pragma unroll
+          for (int c = 0; c < C::kEpiChunks; ++c) {
+            const int col0 = col_base + 32 * c;
+            if (row0 < p.M && col0 < p.N) {
+              if (!epi_lean) epilogue_general_chunk(p, col0, v[c]);
+              if (col0 + 32 <= p.N) {
+#pragma unroll
+                for (int h = 0; h < kBoxes; ++h) {
+                  if (lane == 0) bulk_wait_group_read0();
+                  __syncwarp();
+                  epilogue_stage_box64<C>(stg_row, lane, v[c], h, add);
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  if (lane == 0) {
+                    tma_store_2d_hint(&tmD, stg, col0 + h * kBoxCols, row0, pol_d);
+                    bulk_commit_group();
+                  }
+                }
+              } else if (row < p.M) {
+                epilogue_store_chunk<C, true>(p, row, col0, v[c], add, pol_d);
+              }
+            }
+          }
+        } else if (epi_lean) {
 #pragma unroll
           for (int c = 0; c < C::kEpiChunks; ++c) {
             const int col0 = col_base + 32 * c;

@@ -113,7 +113,8 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
     const int rc = make_tensor_map_2d(
         &tD, C::kBf16Out ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
         args.D, static_cast<uint64_t>(args.N), static_cast<uint64_t>(args.M),
-        static_cast<uint64_t>(args.ldd) * esize, 128 / esize, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+        static_cast<uint64_t>(args.ldd) * esize, C::kStgRowBytes / esize, 32,
+        C::kStgRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc != TG_OK) return rc;
   }
   cudaLaunchConfig_t cfg{};
