@@ -222,6 +222,83 @@ __global__ void __launch_bounds__(128) mma_128x64x64_kernel(const uint16_t* a, c
   }
 }
 
+// ------------------------------------------------- TMEM load shapes
+// "Explicit CUDA tile patterns", section "TMEM transfers": which TMEM cell
+// each register of each lane holds, for the tcgen05.ld shapes.  Four warps
+// fill their 32 TMEM lanes (row = 32 * warp + lane), columns 0..31, with
+// row * 256 + column through tcgen05.st 32x32b, then read columns 0..15 back
+// with 16x64b.x8, 16x128b.x4, 16x256b.x2 and 32x32b.x8 (eight registers each,
+// the 16-lane shapes at the warp's first lane).
+// out: uint32 [4 shapes][128 threads][8 registers].
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+#define TG_LD8(SHAPE)                                                                          \
+  asm volatile("tcgen05.ld.sync.aligned." SHAPE ".b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];" \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),     \
+                 "=r"(r[6]), "=r"(r[7])                                                        \
+               : "r"(taddr)                                                                    \
+               : "memory")
+
+__global__ void __launch_bounds__(128) tmem_shapes_kernel(uint32_t* out) {
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    tmem_alloc<1>(&tmem_slot, 32);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  {
+    uint32_t v[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = static_cast<uint32_t>((warp * 32 + lane) * 256 + c);
+    tmem_st_32x32b_x32(taddr, v);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  uint32_t r[8];
+  TG_LD8("16x64b.x8");
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[(0 * 128 + tid) * 8 + j] = r[j];
+  TG_LD8("16x128b.x4");
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[(1 * 128 + tid) * 8 + j] = r[j];
+  TG_LD8("16x256b.x2");
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[(2 * 128 + tid) * 8 + j] = r[j];
+  TG_LD8("32x32b.x8");
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[(3 * 128 + tid) * 8 + j] = r[j];
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc<1>(tmem, 32);
+  }
+}
+#undef TG_LD8
+
 // ------------------------------------------------- tensor-pipe rate (no memory)
 // One CTA per SM; one thread issues `iters` x 4 back-to-back M128 N256 MMAs
 // (K16 bf16, K32 block-scaled E4M3, or K32 dense E4M3) on shared-memory
@@ -423,6 +500,12 @@ int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, voi
   if (e != cudaSuccess) return cuda_fail(e);
   mma_128x64x64_kernel<<<1, 128, smem, static_cast<cudaStream_t>(s)>>>(a, b, out, ctx->status,
                                                                        wait_timeout_ns());
+  return launched();
+}
+
+int tg_probe_tmem_shapes(uint32_t* out, void* s) {
+  if (!out) return TG_ERR_INVALID_ARG;
+  tmem_shapes_kernel<<<1, 128, 0, static_cast<cudaStream_t>(s)>>>(out);
   return launched();
 }
 

@@ -163,3 +163,22 @@ def test_mma_rate_probe_runs(P, kind, k):
     per_clk = 2 * 128 * 256 * k * 4 * iters / cyc
     nominal = {0: 8192, 1: 16384, 2: 16384}.get(kind, 49152)
     assert per_clk.max() <= 1.05 * nominal
+
+
+def test_tmem_load_shapes_match_the_register_maps(P, oracle):
+    # "Explicit CUDA tile patterns", TMEM transfers: each register of each
+    # lane holds the TMEM cell the page's formula names, for 16x64b, 16x128b,
+    # 16x256b and 32x32b (cells hold row * 256 + column).
+    torch = torch_cuda()
+    out = torch.zeros((4, 128, 8), dtype=torch.int32, device="cuda")
+    P.tmem_shapes(out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint32)
+    for s, shape in enumerate(("16x64b", "16x128b", "16x256b", "32x32b")):
+        want = np.zeros((128, 8), np.uint32)
+        for t in range(128):
+            w, lane = divmod(t, 32)
+            for r in range(8):
+                row, col = oracle.tmem_register_coord(shape, lane, r)
+                want[t, r] = (32 * w + row) * 256 + col
+        assert np.array_equal(got[s], want), shape
