@@ -227,9 +227,10 @@ __global__ void __launch_bounds__(128) mma_128x64x64_kernel(const uint16_t* a, c
 // each register of each lane holds, for the tcgen05.ld shapes.  Four warps
 // fill their 32 TMEM lanes (row = 32 * warp + lane), columns 0..31, with
 // row * 256 + column through tcgen05.st 32x32b, then read columns 0..15 back
-// with 16x64b.x8, 16x128b.x4, 16x256b.x2 and 32x32b.x8 (eight registers each,
-// the 16-lane shapes at the warp's first lane).
-// out: uint32 [4 shapes][128 threads][8 registers].
+// with 16x64b.x8, 16x128b.x4, 16x256b.x2, 32x32b.x8 and 16x32bx2.x8 (eight
+// registers each; the 16-lane shapes at the warp's first lane, the second
+// 16x32bx2 access 16 lanes and 8 columns further).
+// out: uint32 [5 shapes][128 threads][8 registers].
 
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
@@ -290,6 +291,17 @@ __global__ void __launch_bounds__(128) tmem_shapes_kernel(uint32_t* out) {
   tmem_ld_wait();
 #pragma unroll
   for (int j = 0; j < 8; ++j) out[(3 * 128 + tid) * 8 + j] = r[j];
+  // .16x32bx2: the second half-access 16 lanes and 8 columns further
+  // (imm_half_splitoff = (16 << 16) + 8, inside the warp's 32 lanes).
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], 1048584;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[(4 * 128 + tid) * 8 + j] = r[j];
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) {

@@ -73,7 +73,7 @@ def mma_128x64x64(a, b, out, stream=None):
 
 
 def tmem_shapes(out, stream=None):
-    """TMEM cells per register for four tcgen05.ld shapes; out: int32 CUDA [4, 128, 8]."""
+    """TMEM cells per register for five tcgen05.ld shapes; out: int32 CUDA [5, 128, 8]."""
     _check(_L().tg_probe_tmem_shapes(out.data_ptr(), _stream_handle(stream)),
            "tg_probe_tmem_shapes")
 

@@ -59,9 +59,10 @@ int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, voi
 /* "Explicit CUDA tile patterns", section "TMEM transfers": one CTA of four
  * warps writes row * 256 + column into TMEM rows 0..127, columns 0..31
  * (tcgen05.st 32x32b; row = 32 * warp + lane), then reads columns 0..15 back
- * with tcgen05.ld 16x64b.x8, 16x128b.x4, 16x256b.x2 and 32x32b.x8, the
- * 16-lane shapes at each warp's first lane.  out: device uint32
- * [4 shapes][128 threads][8 registers]. */
+ * with tcgen05.ld 16x64b.x8, 16x128b.x4, 16x256b.x2, 32x32b.x8 and
+ * 16x32bx2.x8 (imm_half_splitoff = (16 << 16) + 8), the 16-lane shapes at
+ * each warp's first lane.  out: device uint32 [5 shapes][128 threads][8
+ * registers]. */
 int tg_probe_tmem_shapes(uint32_t* out, void* cuda_stream);
 
 /* Tensor-pipe rate with no memory traffic: `ctas` CTAs (one per SM when

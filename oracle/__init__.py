@@ -429,6 +429,24 @@ def tmem_register_coord(shape: str, lane: int, reg: int) -> tuple[int, int]:
     raise ValueError(f"unknown tcgen05.ld shape {shape!r}")
 
 
+def tmem_register_coord_16x32bx2(lane: int, reg: int, split_lanes: int,
+                                 split_cols: int) -> tuple[int, int]:
+    """(row, column) of TMEM for tcgen05.ld .16x32bx2, relative to the first
+    access region's base, when the second region starts ``split_lanes`` lanes
+    and ``split_cols`` columns further (imm_half_splitoff = split_lanes << 16 |
+    split_cols).
+
+    "Explicit CUDA tile patterns", section "TMEM transfers": lane l owns
+    (access l // 16, row l % 16, column r); each access region is 16 rows by
+    N columns and the second is offset by the immediate alone (no implicit
+    sixteen-row offset).
+    """
+    access, row = divmod(lane, 16)
+    if access == 0:
+        return row, reg
+    return split_lanes + row, split_cols + reg
+
+
 def block_scale_tmem_slot(row: int, sf: int = 0) -> tuple[int, int]:
     """(TMEM lane, byte column) holding scale ``sf`` of scale row ``row``.
 

@@ -490,6 +490,20 @@ def test_tmem_register_images_are_bijections(oracle, shape, rows, regs_per_x):
         assert {c[1] for c in cells} == set(range(C))
 
 
+def test_tmem_16x32bx2_matches_the_page_example(oracle):
+    # The page's .16x32bx2.x4 example with imm_half_splitoff = (16 << 16) + 8
+    # reads memory[:, :16, :4] and memory[:, 16:32, 8:12]: lanes 0..15 the
+    # first block, lanes 16..31 the second, four registers each.
+    cells = {(l, r): oracle.tmem_register_coord_16x32bx2(l, r, 16, 8)
+             for l in range(32) for r in range(4)}
+    low = {cells[(l, r)] for l in range(16) for r in range(4)}
+    high = {cells[(l, r)] for l in range(16, 32) for r in range(4)}
+    assert low == {(i, j) for i in range(16) for j in range(4)}
+    assert high == {(i, j) for i in range(16, 32) for j in range(8, 12)}
+    # no implicit sixteen-row offset: a zero lane offset reuses rows 0..15
+    assert oracle.tmem_register_coord_16x32bx2(16, 0, 0, 8) == (0, 8)
+
+
 def test_block_scale_slots_cover_128_rows(oracle):
     slots = [oracle.block_scale_tmem_slot(r) for r in range(128)]
     assert len(set(slots)) == 128

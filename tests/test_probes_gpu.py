@@ -168,17 +168,20 @@ def test_mma_rate_probe_runs(P, kind, k):
 def test_tmem_load_shapes_match_the_register_maps(P, oracle):
     # "Explicit CUDA tile patterns", TMEM transfers: each register of each
     # lane holds the TMEM cell the page's formula names, for 16x64b, 16x128b,
-    # 16x256b and 32x32b (cells hold row * 256 + column).
+    # 16x256b, 32x32b and 16x32bx2 (cells hold row * 256 + column).
     torch = torch_cuda()
-    out = torch.zeros((4, 128, 8), dtype=torch.int32, device="cuda")
+    out = torch.zeros((5, 128, 8), dtype=torch.int32, device="cuda")
     P.tmem_shapes(out)
     torch.cuda.synchronize()
     got = out.cpu().numpy().view(np.uint32)
-    for s, shape in enumerate(("16x64b", "16x128b", "16x256b", "32x32b")):
+    for s, shape in enumerate(("16x64b", "16x128b", "16x256b", "32x32b", "16x32bx2")):
         want = np.zeros((128, 8), np.uint32)
         for t in range(128):
             w, lane = divmod(t, 32)
             for r in range(8):
-                row, col = oracle.tmem_register_coord(shape, lane, r)
+                if shape == "16x32bx2":
+                    row, col = oracle.tmem_register_coord_16x32bx2(lane, r, 16, 8)
+                else:
+                    row, col = oracle.tmem_register_coord(shape, lane, r)
                 want[t, r] = (32 * w + row) * 256 + col
         assert np.array_equal(got[s], want), shape
