@@ -154,6 +154,19 @@ __global__ void tma_swizzle_kernel(const __grid_constant__ CUtensorMap map, int 
 }
 
 // ---------------------------------------------------- tcgen05 128x64x64 example
+// Weight-stationary form ("tcgen05.mma", Block-scaled opcodes and .ws: M128
+// .ws uses the same TMEM layout D as M128 without .ws; CTA group 1, N 64).
+__device__ __forceinline__ void mma_ws_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <bool kWs>
 __global__ void __launch_bounds__(128) mma_128x64x64_kernel(const uint16_t* a, const uint16_t* b,
                                                             float* out, uint32_t* status,
                                                             uint64_t timeout_ns) {
@@ -192,10 +205,14 @@ __global__ void __launch_bounds__(128) mma_128x64x64_kernel(const uint16_t* a, c
   if (tid == 0) {
     const uint32_t a0 = smem_addr(sa), b0 = smem_addr(sb);
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      mma_bf16<1>(tmem, make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B),
-                  make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B),
-                  idesc_bf16_f32(128, 64), k != 0);
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t ad = make_smem_desc(a0 + 32 * k, 16, 1024, kDescSwizzle128B);
+      const uint64_t bd = make_smem_desc(b0 + 32 * k, 16, 1024, kDescSwizzle128B);
+      if constexpr (kWs)
+        mma_ws_bf16(tmem, ad, bd, idesc_bf16_f32(128, 64), k != 0);
+      else
+        mma_bf16<1>(tmem, ad, bd, idesc_bf16_f32(128, 64), k != 0);
+    }
     mma_commit(&bar);
   }
   __syncwarp();
@@ -419,6 +436,23 @@ __global__ void wait_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
 
 using namespace tg;
 
+namespace {
+template <bool kWs>
+int launch_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, void* s) {
+  if (!a || !b || !out) return TG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b)) return TG_ERR_MISALIGNED;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  const int smem = 128 * 128 + 64 * 128 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mma_128x64x64_kernel<kWs>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  mma_128x64x64_kernel<kWs><<<1, 128, smem, static_cast<cudaStream_t>(s)>>>(
+      a, b, out, ctx->status, wait_timeout_ns());
+  return launched();
+}
+}  // namespace
+
 extern "C" {
 
 int tg_probe_add_one_v4(const float* a, float* b, void* s) {
@@ -501,18 +535,13 @@ int tg_probe_tma_swizzle128(const uint16_t* src, int rows, uint8_t* out, void* s
   return launched();
 }
 
+
 int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, void* s) {
-  if (!a || !b || !out) return TG_ERR_INVALID_ARG;
-  if (!aligned16(a) || !aligned16(b)) return TG_ERR_MISALIGNED;
-  DeviceCtx* ctx = current_ctx();
-  if (!ctx) return TG_ERR_CUDA;
-  const int smem = 128 * 128 + 64 * 128 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(mma_128x64x64_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return cuda_fail(e);
-  mma_128x64x64_kernel<<<1, 128, smem, static_cast<cudaStream_t>(s)>>>(a, b, out, ctx->status,
-                                                                       wait_timeout_ns());
-  return launched();
+  return launch_mma_128x64x64<false>(a, b, out, s);
+}
+
+int tg_probe_mma_ws_128x64x64(const uint16_t* a, const uint16_t* b, float* out, void* s) {
+  return launch_mma_128x64x64<true>(a, b, out, s);
 }
 
 int tg_probe_tmem_shapes(uint32_t* out, void* s) {

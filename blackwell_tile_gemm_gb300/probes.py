@@ -25,6 +25,7 @@ def _L():
             "tg_probe_tma_two_boxes": [vp, vp, vp],
             "tg_probe_tma_swizzle128": [vp, i32, vp, vp],
             "tg_probe_mma_128x64x64": [vp, vp, vp, vp],
+            "tg_probe_mma_ws_128x64x64": [vp, vp, vp, vp],
             "tg_probe_wait_timeout": [ctypes.c_uint64, vp],
             "tg_probe_mma_rate": [i32, i32, i32, vp, vp],
             "tg_probe_tmem_shapes": [vp, vp],
@@ -76,6 +77,11 @@ def tmem_shapes(out, stream=None):
     """TMEM cells per register for five tcgen05.ld shapes; out: int32 CUDA [5, 128, 8]."""
     _check(_L().tg_probe_tmem_shapes(out.data_ptr(), _stream_handle(stream)),
            "tg_probe_tmem_shapes")
+
+
+def mma_ws_128x64x64(a, b, out, stream=None):
+    _check(_L().tg_probe_mma_ws_128x64x64(a.data_ptr(), b.data_ptr(), out.data_ptr(),
+                                          _stream_handle(stream)), "tg_probe_mma_ws_128x64x64")
 
 
 def wait_timeout(timeout_ns, stream=None):

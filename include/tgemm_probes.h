@@ -56,6 +56,12 @@ int tg_probe_tma_swizzle128(const uint16_t* src, int rows, uint8_t* out, void* c
  * warps read TMEM back with tcgen05.ld 32x32b; out: f32 [128, 64] = a @ b.T. */
 int tg_probe_mma_128x64x64(const uint16_t* a, const uint16_t* b, float* out, void* cuda_stream);
 
+/* The same example with the weight-stationary opcode ("tcgen05.mma": M128
+ * .ws uses TMEM layout D like M128 without .ws; CTA group 1, N = 64):
+ * tcgen05.mma.ws.cta_group::1.kind::f16, same operands and read-back. */
+int tg_probe_mma_ws_128x64x64(const uint16_t* a, const uint16_t* b, float* out,
+                              void* cuda_stream);
+
 /* "Explicit CUDA tile patterns", section "TMEM transfers": one CTA of four
  * warps writes row * 256 + column into TMEM rows 0..127, columns 0..31
  * (tcgen05.st 32x32b; row = 32 * warp + lane), then reads columns 0..15 back

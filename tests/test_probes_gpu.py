@@ -87,22 +87,24 @@ def test_tma_swizzle128_image(P, oracle, rows):
     assert np.array_equal(got, want)
 
 
-def _mma(P, a_bits, b_bits):
+def _mma(P, a_bits, b_bits, ws=False):
     torch = torch_cuda()
     out = torch.full((128, 64), float("nan"), dtype=torch.float32, device="cuda")
-    P.mma_128x64x64(dev_bf16(a_bits), dev_bf16(b_bits), out)
+    (P.mma_ws_128x64x64 if ws else P.mma_128x64x64)(dev_bf16(a_bits), dev_bf16(b_bits), out)
     import blackwell_tile_gemm_gb300 as tg
     assert tg.tg_device_status()[0] == tg.TG_OK
     return out.cpu().numpy().astype(np.float64)
 
 
-def test_mma_worked_example_128x64x64(P, oracle):
+@pytest.mark.parametrize("ws", [False, True], ids=["mma", "mma.ws"])
+def test_mma_worked_example_128x64x64(P, oracle, ws):
     # The page's data: default_rng(0), randint(-4, 5) / 4 for a (128, 64) and
     # b (64, 64), B stored as (N, K); checked as a @ b.T at rtol = atol = 2e-4.
+    # With .ws the M128 result uses the same TMEM layout, so the same check.
     rng = np.random.default_rng(0)
     a = synth.f32_to_bf16_bits((rng.integers(-4, 5, (128, 64)) / 4).astype(np.float32))
     b = synth.f32_to_bf16_bits((rng.integers(-4, 5, (64, 64)) / 4).astype(np.float32))
-    got = _mma(P, a, b)
+    got = _mma(P, a, b, ws)
     ref, _ = oracle.gemm_bf16(a, b)
     np.testing.assert_allclose(got, ref, rtol=2e-4, atol=2e-4)
     assert np.array_equal(got, ref)      # quarter integers: every partial sum is exact
