@@ -16,6 +16,17 @@ they are used again, so no separate L2 flush is inserted.
 ``--impl reference`` times the CPU oracle (float64, the machine's host cores) on
 a bounded sample of the same workload per step and prints the same JSON
 line with "impl": "reference".
+
+The library is single-GPU code (one process drives one GPU; its short-K and
+opt-in kernels use TMA multicast within that GPU's clusters).  ``--gpus N``
+with N > 1, or a launch with WORLD_SIZE > 1, does no GPU work: rank 0 prints
+one line saying so and every rank exits 0.
+
+The line also carries what checks the timed work: the oracle's values on the
+CPU-baseline sample compared with the last timed step's outputs
+("parity"), the SM clock sampled while each kernel ran, and the fraction of
+the tensor pipe's own rate (SMs x FLOP per SM per clock from the rate probe x
+that clock).
 """
 from __future__ import annotations
 
@@ -110,65 +121,170 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+def gpu_ids(torch, dev_index):
+    """(uuid string "GPU-...", or None) of the CUDA device, for NVML / nvidia-smi."""
+    try:
+        u = getattr(torch.cuda.get_device_properties(dev_index), "uuid", None)
+    except Exception:               # noqa: BLE001
+        u = None
+    if u is None:
+        return None
+    u = str(u)
+    return u if u.startswith("GPU-") else "GPU-" + u
 
+
+class ClockSampler:
+    """SM clock and throttle reasons sampled during the timed region, with host
+    timestamps (time.perf_counter), so that each sample can be attributed to
+    the kernel that was running.  NVML (read-only queries through the
+    driver's libnvidia-ml) every ~1 ms; else nvidia-smi every 100 ms."""
+
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
-        self.gpu = gpu_index
+    def __init__(self, uuid, index: int, period_ms: float = 1.0):
+        self.uuid = uuid
+        self.index = index
         self.period = period_ms
-        self.proc = None
-        self.lines = []
+        self.samples = []          # (host time, sm MHz, max sm MHz, set of reasons)
+        self.source = None
+        self._stop = threading.Event()
         self._t = None
+        self._proc = None
+
+    def _nvml(self):
+        import ctypes
+        try:
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if L.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = L.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = L.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) == 0
+        if not ok:
+            return None
+        reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        return L, h, reasons
 
     def __enter__(self):
+        import ctypes
+        nv = self._nvml()
+        if nv is not None:
+            L, h, reasons_fn = nv
+            self.source = "nvml"
+            smax = ctypes.c_uint(0)
+            L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(smax))
+
+            def loop():
+                c = ctypes.c_uint(0)
+                m = ctypes.c_ulonglong(0)
+                while not self._stop.is_set():
+                    t = time.perf_counter()
+                    if L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0:
+                        rs = set()
+                        if reasons_fn is not None and reasons_fn(h, ctypes.byref(m)) == 0:
+                            rs = {n for b, n in self.REASON_BITS.items() if m.value & b}
+                        self.samples.append((t, float(c.value), float(smax.value), rs))
+                    time.sleep(self.period * 1e-3)
+            self._t = threading.Thread(target=loop, daemon=True)
+            self._t.start()
+            return self
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+            ident = self.uuid or str(self.index)
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms=100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi"
+
+            def read():
+                names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                         "sw_power_cap"]
+                for line in self._proc.stdout:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm, smax = float(parts[1]), float(parts[2])
+                    except ValueError:
+                        continue
+                    rs = {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}
+                    self.samples.append((time.perf_counter(), sm, smax, rs))
+            self._t = threading.Thread(target=read, daemon=True)
             self._t.start()
         except (OSError, ValueError):
-            self.proc = None
+            self._proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-            if self._t is not None:
-                self._t.join(timeout=5)
+                self._proc.kill()
+        if self._t is not None:
+            self._t.join(timeout=5)
+
+    @staticmethod
+    def _summary(samples):
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for x in samples:
+            reasons |= x[3]
+        return {"sm_mhz": statistics.median(x[1] for x in samples),
+                "sm_max_mhz": max(x[2] for x in samples), "reasons": sorted(reasons),
+                "samples": len(samples)}
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        d = self._summary(self.samples)
+        d["source"] = self.source
+        return d
+
+    def per_interval(self, t0_host: float, intervals):
+        """Median clock of the samples that fall in each named interval.
+
+        intervals: {name: [(start_ms, end_ms), ...]} on the device timeline,
+        relative to an event recorded on an idle stream at host time t0_host."""
+        out = {}
+        for name, ivs in intervals.items():
+            got = []
+            for x in self.samples:
+                g = (x[0] - t0_host) * 1e3
+                if any(a <= g < b for a, b in ivs):
+                    got.append(x)
+            out[name] = self._summary(got)
+        return out
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 # ---------------------------------------------------------------------------
@@ -199,7 +315,24 @@ def make_step_inputs(torch, dev):
     return host, d
 
 
-def run_ours(args, rank, world, local):
+def probe_rates(torch, dev):
+    """Dense FLOP per SM per clock of the tensor pipe, measured live by the
+    library's rate probe (back-to-back MMAs on every SM, no memory traffic):
+    bf16 kind::f16 and E4M3 block-scaled kind::mxf8f6f4."""
+    from blackwell_tile_gemm_gb300 import probes
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {}
+    for name, kind, k in (("bf16", 0, 16), ("mxfp8", 1, 32)):
+        iters = 2048
+        cyc = torch.zeros(2 * sms, dtype=torch.int64, device=dev)
+        probes.mma_rate(kind, iters, sms, cyc)
+        torch.cuda.synchronize()
+        c = cyc.view(sms, 2)[:, 0].double().median().item()
+        out[name] = 2 * 128 * 256 * k * 4 * iters / c
+    return sms, out
+
+
+def run_ours(args):
     import torch
 
     import blackwell_tile_gemm_gb300 as tg
@@ -208,8 +341,8 @@ def run_ours(args, rank, world, local):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
     tgbuild.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     host, d = make_step_inputs(torch, dev)
     flops_gemm = 2 * SIZE ** 3
@@ -246,6 +379,7 @@ def run_ours(args, rank, world, local):
         if ev is not None:
             ev[3].record(stream)
 
+    sms, rates = probe_rates(torch, dev)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -253,50 +387,73 @@ def run_ours(args, rank, world, local):
     if code != tg.TG_OK:
         raise SystemExit(f"device status {code} (site {site}) during warm-up")
 
-    barrier(world)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(gpu_ids(torch, 0), 0) as clk:
+        time.sleep(0.005)                 # a few idle samples before the region
+        h0 = time.perf_counter()          # the stream is idle: t_start runs at once
         t_start.record(stream)
         for k in range(args.steps):
             step(evs[k])
         t_end.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
+        time.sleep(0.002)
     total_ms = t_start.elapsed_time(t_end)
     code, site = tg.tg_device_status()
     if code != tg.TG_OK:
         raise SystemExit(f"device status {code} (site {site}) in the timed region")
     per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
                     for e in evs])
-    total_ms = reduce_max(total_ms, world)
+    # Each kernel's intervals on the device timeline (ms after t_start), to
+    # attribute the clock samples.
+    starts = np.array([[t_start.elapsed_time(e[i]) for i in range(4)] for e in evs])
     ms_step = total_ms / args.steps
     if flops_step:
-        value = flops_step * world / (ms_step * 1e-3) / 1e12
+        value = flops_step / (ms_step * 1e-3) / 1e12
     else:   # transpose alone: report its bandwidth instead
-        value = 2 * 2 * SIZE * SIZE * world / (ms_step * 1e-3) / 1e9
+        value = 2 * 2 * SIZE * SIZE / (ms_step * 1e-3) / 1e9
 
     peaks, peak_src = measured_peaks()
     bf16_ms, mx_ms, tr_ms = (float(per[:, i].mean()) for i in range(3))
     peak_bf16 = float(peaks["bf16_tflops"])
+    names = ["gemm_bf16", f"{args.kernel}_blockscaled" if run_f4 else "gemm_mxfp8_blockscaled",
+             "tile_transpose_b16"]
+    clk_by_kernel = clk.per_interval(h0, {
+        n: [(float(starts[k, i]), float(starts[k, i + 1])) for k in range(args.steps)]
+        for i, n in enumerate(names)})
+
+    def theoretical(tflops, rate, mhz):
+        if not mhz:
+            return None
+        return tflops * 1e12 / (sms * rate * mhz * 1e6)
+
     kern = {}
     if run_bf16:
         t = flops_gemm / (bf16_ms * 1e-3) / 1e12
-        kern["gemm_bf16"] = {"ms": bf16_ms, "tflops": t, "frac_of_bf16_peak": t / peak_bf16}
+        c = clk_by_kernel["gemm_bf16"]
+        kern["gemm_bf16"] = {"ms": bf16_ms, "tflops": t, "frac_of_bf16_peak": t / peak_bf16,
+                             "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"],
+                             "frac_theoretical": theoretical(t, rates["bf16"], c["sm_mhz"])}
     if run_mx:
         t = flops_gemm / (mx_ms * 1e-3) / 1e12
-        kern["gemm_mxfp8_blockscaled"] = {"ms": mx_ms, "tflops": t,
-                                          "frac_of_2x_bf16_peak": t / (2 * peak_bf16)}
+        c = clk_by_kernel["gemm_mxfp8_blockscaled"]
+        kern["gemm_mxfp8_blockscaled"] = {
+            "ms": mx_ms, "tflops": t, "frac_of_2x_bf16_peak": t / (2 * peak_bf16),
+            "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"],
+            "frac_theoretical": theoretical(t, rates["mxfp8"], c["sm_mhz"])}
     if run_f4:
         t = flops_gemm / (mx_ms * 1e-3) / 1e12
-        kern[f"{args.kernel}_blockscaled"] = {"ms": mx_ms, "tflops": t,
-                                              "frac_of_6x_bf16_peak": t / (6 * peak_bf16)}
+        c = clk_by_kernel[names[1]]
+        kern[names[1]] = {"ms": mx_ms, "tflops": t, "frac_of_6x_bf16_peak": t / (6 * peak_bf16),
+                          "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"]}
     if run_tr:
         g = 2 * 2 * SIZE * SIZE / (tr_ms * 1e-3) / 1e9
+        c = clk_by_kernel["tile_transpose_b16"]
         kern["tile_transpose_b16"] = {"ms": tr_ms, "gbs": g,
-                                      "frac_of_hbm_peak": g / float(peaks["hbm_gbs"])}
+                                      "frac_of_hbm_peak": g / float(peaks["hbm_gbs"]),
+                                      "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"]}
     dominant = max(kern, key=lambda n: kern[n]["ms"])
     if dominant == "tile_transpose_b16":
         achieved, peak = kern[dominant]["gbs"], float(peaks["hbm_gbs"])
@@ -316,14 +473,31 @@ def run_ours(args, rank, world, local):
                 "frac": achieved / peak,
                 "traffic": profiled_traffic(dominant) if SIZE == 8192 else None,
                 "peak_source": peak_note}
+    if dominant in ("gemm_bf16", "gemm_mxfp8_blockscaled"):
+        rate = rates["bf16" if dominant == "gemm_bf16" else "mxfp8"]
+        mhz = kern[dominant]["sm_mhz"]
+        max_mhz = clk.summary()["sm_max_mhz"] or 2070.0
+        roofline.update({
+            "frac_theoretical": theoretical(achieved, rate, mhz),
+            "theoretical_peak": sms * rate * mhz * 1e6 / 1e12 if mhz else None,
+            "frac_theoretical_at_max_clock": theoretical(achieved, rate, max_mhz),
+            "theoretical_basis": (f"{sms} SMs x {rate:.0f} FLOP/clk/SM (rate probe, "
+                                  f"back-to-back tcgen05.mma) x the median SM clock sampled "
+                                  f"while the kernel ran ({mhz} MHz)")})
 
+    # Check the timed work: the last step's outputs against the oracle on the
+    # CPU-baseline sample (and the transpose against a host transpose).
+    parity = None
+    cpu = None
+    if args.kernel == "all":
+        cpu, samples = cpu_baseline(args.cpu_seconds)
+        parity = step_parity(torch, d, host, samples)
     e2e = measure_e2e(torch, tg, host, dev, stream, args.e2e_steps if args.kernel == "all" else 0,
                       flops_step)
-    cpu = cpu_baseline(args.cpu_seconds) if (rank == 0 and world == 1 and args.cpu_seconds > 0) \
-        else None
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT if flops_step else "GB/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT if flops_step else "GB/s", "n_gpus": 1,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "e2m1 (f32 accumulate)" if run_f4 else "bf16+e4m3 (f32 accumulate)",
@@ -331,17 +505,40 @@ def run_ours(args, rank, world, local):
         "config": {"workload": workload() if args.kernel == "all" else f"{args.kernel} only",
                    "M": SIZE, "N": SIZE, "K": SIZE,
                    "tiles": "256x256 per CTA pair, 128-byte K stages",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": "single GPU",
                    "l2": "not flushed: 516 MB of step inputs > 129 MB L2"},
         "roofline": roofline, "kernels": kern, "e2e": e2e,
         "gpu_launches": (int(run_bf16) + 2 * int(run_mx) + 2 * int(run_f4) + int(run_tr))
         * args.steps,
         "clocks": clk.summary(),
+        "tensor_pipe_probe": {"sms": sms, "flop_per_clk_per_sm": rates},
     }
+    if parity is not None:
+        line["parity"] = parity
     if cpu is not None:
         line["cpu_baseline"] = cpu
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    print(json.dumps(line), flush=True)
+
+
+def step_parity(torch, d, host, samples):
+    """Worst |D - ref| / tol of the timed step's GEMM outputs on the oracle's
+    sample, and whether the transpose equals the host transpose bit for bit."""
+    rows, cols, ref_b, mag_b, ref_m, mag_m = samples
+    r_t = torch.from_numpy(rows).to(d["D"].device)
+    got_b = d["D"].index_select(0, r_t).cpu().numpy().astype(np.float64)[:, cols]
+    bits = d["mD"].view(torch.int16).index_select(0, r_t).cpu().numpy().view(np.uint16)[:, cols]
+    got_m = synth.bf16_bits_to_f32(bits).astype(np.float64)
+    # |D - ref| <= rtol * sum_k |a_k b_k| + atol: f32 D (bf16 GEMM), bf16 D (MXFP8)
+    rb = float(np.max(np.abs(got_b - ref_b) / (1e-5 * mag_b + 1e-6)))
+    rm = float(np.max(np.abs(got_m - ref_m) / (8e-3 * mag_m + 1e-3)))
+    if not (np.all(np.isfinite(got_b)) and np.all(np.isfinite(got_m))):
+        rb = rm = float("inf")
+    xt = d["XT"].cpu().numpy().view(np.uint16)
+    tr_ok = bool(np.array_equal(xt, host["tr"]["X"].T))
+    return {"max_err_over_tol": max(rb, rm), "gemm_bf16": rb, "gemm_mxfp8_blockscaled": rm,
+            "transpose_bit_exact": tr_ok,
+            "sample": f"{rows.size} rows x {cols.size} columns of each GEMM's D from the last "
+                      f"timed step vs the float64 oracle; transpose: every element"}
 
 
 def measure_e2e(torch, tg, host, dev, stream, steps, flops_step):
@@ -587,35 +784,59 @@ def _oracle_sample_inputs():
 
 def oracle_sample(rows_per_gemm: int, cols: int, offset: int):
     """Oracle on `rows_per_gemm` full-K rows x `cols` columns of each 8192^3
-    GEMM; returns (flops, seconds)."""
+    GEMM; returns (flops, seconds, (rows, cols, ref, mag of bf16, ref, mag of
+    MXFP8))."""
     import oracle
     x = _oracle_sample_inputs()
-    rows = (np.arange(rows_per_gemm) * 61 + offset) % SIZE
-    cs = (np.arange(cols) * 37 + offset) % SIZE
+    rows = np.unique((np.arange(rows_per_gemm) * 61 + offset) % SIZE)
+    cs = np.unique((np.arange(cols) * 37 + offset) % SIZE)
     t0 = time.perf_counter()
-    oracle.gemm_bf16(x["bf16"]["A"], x["bf16"]["B"], rows=rows, cols=cs)
-    oracle.gemm_mxfp8(x["mx"]["A"], x["mx"]["B"], x["mx"]["SFA"], x["mx"]["SFB"],
-                      rows=rows, cols=cs)
+    rb, mb = oracle.gemm_bf16(x["bf16"]["A"], x["bf16"]["B"], rows=rows, cols=cs)
+    rm, mm = oracle.gemm_mxfp8(x["mx"]["A"], x["mx"]["B"], x["mx"]["SFA"], x["mx"]["SFB"],
+                               rows=rows, cols=cs)
     dt = time.perf_counter() - t0
-    return 2 * 2 * rows_per_gemm * cols * SIZE, dt
+    return 2 * 2 * rows.size * cs.size * SIZE, dt, (rows, cs, rb, mb, rm, mm)
+
+
+def single_thread_tiny():
+    """The oracle on one thread for the 128 x 128 x 256 bf16 product (f32 D):
+    median seconds of 5 runs."""
+    import oracle
+    x = synth.make_inputs("tiny")
+    n = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        times = []
+        for _ in range(5):
+            t0 = time.perf_counter()
+            oracle.gemm_bf16(x["A"], x["B"])
+            times.append(time.perf_counter() - t0)
+    finally:
+        oracle.set_num_threads(n)
+    return statistics.median(times)
 
 
 def cpu_baseline(target_seconds: float):
-    """The oracle on a growing sample until one run takes about target_seconds."""
+    """The oracle on a growing sample until one run takes about target_seconds;
+    returns (the cpu_baseline object, the last sample's oracle values)."""
     import oracle
     oracle.build()
     _oracle_sample_inputs()
     cores = oracle.num_threads()
     cols = min(1024, SIZE)
     rows = max(cores, 16)
-    flops, dt = oracle_sample(rows, cols, 0)
+    flops, dt, samples = oracle_sample(rows, cols, 0)
     while dt < 0.6 * target_seconds and rows < SIZE:
         rows = min(SIZE, rows * 2)
-        flops, dt = oracle_sample(rows, cols, rows)
+        flops, dt, samples = oracle_sample(rows, cols, rows)
+    t1 = single_thread_tiny()
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "seconds": dt,
-            "sample": (f"float64 oracle on {rows} rows x {cols} columns (all K = {SIZE}) of each "
-                       f"{SIZE}^3 GEMM (bf16 and MXFP8), operands decoded per call")}
+            "seconds": dt, "cpu_model": cpu_model(),
+            "single_thread": {"workload": "bf16 128x128x256, f32 D (the tiny workload)",
+                              "seconds": t1, "gflops": 2 * 128 * 128 * 256 / t1 / 1e9},
+            "sample": (f"float64 oracle on {samples[0].size} rows x {samples[1].size} columns "
+                       f"(all K = {SIZE}) of each {SIZE}^3 GEMM (bf16 and MXFP8), operands "
+                       f"decoded per call")}, samples
 
 
 def run_reference(args, rank, world):
@@ -631,7 +852,7 @@ def run_reference(args, rank, world):
     flops = 0.0
     secs = 0.0
     for k in range(args.steps):
-        f, dt = oracle_sample(rows, cols, k + 1)
+        f, dt, _ = oracle_sample(rows, cols, k + 1)
         flops += f
         secs += dt
     value = flops / secs / 1e12
@@ -646,46 +867,10 @@ def run_reference(args, rank, world):
                    "M": SIZE, "N": SIZE, "K": SIZE,
                    "parallelism": "host cores (OpenMP over output rows)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-# ---------------------------------------------------------------------------
-# multi-process plumbing (one process per GPU; replicas, no data exchange)
-# ---------------------------------------------------------------------------
-
-_PG = {"init": False}
-
-
-def init_dist(world, local):
-    if world <= 1:
-        return
-    import torch
-    import torch.distributed as dist
-    backend = "nccl" if torch.cuda.is_available() else "gloo"
-    if torch.cuda.is_available():
-        torch.cuda.set_device(local)
-    dist.init_process_group(backend=backend)
-    _PG["init"] = True
-
-
-def barrier(world):
-    if world > 1 and _PG["init"]:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def reduce_max(x: float, world: int) -> float:
-    if world <= 1 or not _PG["init"]:
-        return x
-    import torch
-    import torch.distributed as dist
-    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
 
 
 def main(argv=None):
@@ -712,20 +897,24 @@ def main(argv=None):
         ap.error("--size must be a positive multiple of 256")
     global SIZE
     SIZE = args.size
-    rank, world, local = dist_env()
+    rank, world, _ = dist_env()
+    if args.impl == "reference":
+        # the oracle on host cores: rank 0 only, whatever the launch
+        run_reference(args, rank, world)
+        return
+    if args.gpus > 1 or world > 1:
+        # Single-GPU library: no multi-GPU run (its multicast TMA kernels are
+        # 1-GPU code), so nothing is launched on any GPU.
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "n_gpus": max(args.gpus, world),
+                              "unavailable": "the library is single-GPU code (one process "
+                                             "drives one GPU); run bench.py with --gpus 1"}),
+                  flush=True)
+        return
     if args.configs:
         run_configs(args)
         return
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        return
-    init_dist(world, local)
-    try:
-        run_ours(args, rank, world, local)
-    finally:
-        if _PG["init"]:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+    run_ours(args)
 
 
 if __name__ == "__main__":

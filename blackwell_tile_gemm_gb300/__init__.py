@@ -29,6 +29,7 @@ TG_ERR_UNSUPPORTED = 3
 TG_ERR_CUDA = 4
 TG_ERR_TIMEOUT = 5
 TG_ERR_NO_SCRATCH = 6
+TG_ERR_WORKSPACE = 7
 TG_D_F32 = 0
 TG_D_BF16 = 1
 TG_EPI_NONE = 0
@@ -40,6 +41,12 @@ TG_EPI_AFFINE = 5
 TG_FLAG_CTA_PAIR = 1
 TG_FLAG_MULTICAST = 2
 TG_FLAG_GATHER_TMA = 4
+TG_CALL_GEMM_BF16 = 0
+TG_CALL_GEMM_MXFP8 = 1
+TG_CALL_GEMM_MXFP4 = 2
+TG_CALL_GEMM_NVFP4 = 3
+TG_CALL_GEMM_BF16_SKINNY = 4
+TG_CALL_GEMM_BF16_GATHER = 5
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +108,14 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(tg_epilogue), u32, vp]
         L.tg_gemm_tail_split.restype = i32
         L.tg_gemm_tail_split.argtypes = [i64, i64, i64, u32]
+        L.tg_gemm_multicast.restype = i32
+        L.tg_gemm_multicast.argtypes = [vp, vp, i64, i64, i64, u32]
+        L.tg_workspace_bytes.restype = i64
+        L.tg_workspace_bytes.argtypes = [i32, i64, i64, i64, i64, i64, i32, i32, u32]
+        L.tg_reserve_workspace.restype = i32
+        L.tg_reserve_workspace.argtypes = [vp, i64]
+        L.tg_workspace_alloc_count.restype = ctypes.c_uint64
+        L.tg_workspace_alloc_count.argtypes = []
         L.tg_gemm_repitch.restype = i32
         L.tg_gemm_repitch.argtypes = [i64, i64, i64, i64, i64]
         L.tg_skinny_split_count.restype = i32
@@ -348,6 +363,44 @@ def gemm_tail_split(M: int, N: int, K: int, cta_pair: bool = False) -> int:
     if r < 0:
         raise TgError(-r, "tg_gemm_tail_split")
     return r
+
+
+def _addr(x):
+    """Device address of a tensor, or an integer address as given."""
+    return int(x) if isinstance(x, int) else x.data_ptr()
+
+
+def gemm_multicast(A, B, M: int, N: int, K: int, cta_pair: bool = False,
+                   multicast: bool = False) -> bool:
+    """Whether gemm_bf16 runs multicast clusters for these operands (tensors or
+    raw addresses), sizes and flags; False unless A and B are allocations of
+    the current device.  Reads pointer attributes only."""
+    r = lib().tg_gemm_multicast(_addr(A), _addr(B), int(M), int(N), int(K),
+                                _flags(cta_pair, multicast))
+    if r < 0:
+        raise TgError(-r, "tg_gemm_multicast")
+    return bool(r)
+
+
+def workspace_bytes(call: int, M: int, N: int, K: int, lda: int = 0, ldb: int = 0,
+                    d_dtype: int = TG_D_F32, epi_op: int = TG_EPI_NONE, flags: int = 0) -> int:
+    """Stream workspace bytes one call of kind ``call`` (TG_CALL_*) needs."""
+    r = lib().tg_workspace_bytes(int(call), int(M), int(N), int(K), int(lda), int(ldb),
+                                 int(d_dtype), int(epi_op), int(flags))
+    if r < 0:
+        raise TgError(int(-r), "tg_workspace_bytes")
+    return int(r)
+
+
+def reserve_workspace(nbytes: int, stream=None) -> None:
+    """Allocate the stream's workspace (>= nbytes) and tail scratch now; later
+    calls on the stream then neither allocate nor synchronise."""
+    _check(lib().tg_reserve_workspace(_stream_handle(stream), int(nbytes)), "tg_reserve_workspace")
+
+
+def workspace_alloc_count() -> int:
+    """Device allocations the library has made since it was loaded."""
+    return int(lib().tg_workspace_alloc_count())
 
 
 def gemm_repitch(M: int, N: int, K: int, lda: int, ldb: int) -> int:

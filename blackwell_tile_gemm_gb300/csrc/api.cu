@@ -33,13 +33,24 @@ DeviceCtx g_ctx[kMaxDevices];
 uint64_t g_timeout_ns = 2000000000ull;
 thread_local int t_last_cuda_error = 0;
 
-struct Workspace {
-  void* ptr = nullptr;
-  size_t bytes = 0;
+// Library-owned device memory of one (device, stream): calls on different
+// streams never share it, and calls on one stream are ordered.
+//   ws        the workspace (scale images, re-pitched or gathered rows, the
+//             skinny call's partial sums), grown on demand unless reserved;
+//   partials, counters  the tail split's partial tiles and arrival counters;
+//   reserved  set by tg_reserve_workspace: from then on no call on this
+//             stream allocates or synchronises; a call that would need more
+//             workspace returns TG_ERR_WORKSPACE instead.
+struct StreamState {
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  float* partials = nullptr;
+  uint32_t* counters = nullptr;
+  bool reserved = false;
 };
-// One workspace per (device, stream): calls on different streams never
-// share one, and calls on one stream are ordered.
-std::map<std::pair<int, uintptr_t>, Workspace> g_workspace;
+std::map<std::pair<int, uintptr_t>, StreamState> g_streams;
+// Device allocations the library has made (workspace, tail scratch).
+uint64_t g_alloc_count = 0;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -163,36 +174,88 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
 }
 
 namespace {
-struct TailScratch {
-  float* partials = nullptr;
-  uint32_t* flags = nullptr;
-};
-std::map<std::pair<int, uintptr_t>, TailScratch> g_tail;
+
+std::pair<int, uintptr_t> stream_key(int dev, cudaStream_t stream) {
+  return std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+}
+
+// True when `stream` is being captured into a graph, or when its capture
+// state cannot be read (the legacy stream while another stream captures):
+// an allocation or a synchronisation then would break the capture.
+bool stream_capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) {
+    cudaGetLastError();
+    return true;
+  }
+  return st != cudaStreamCaptureStatusNone;
+}
+
+// Allocates the tail scratch of `t` (zeroed counters, ordered on `stream`).
+// Caller holds g_mutex.
+bool alloc_tail_scratch(StreamState& t, cudaStream_t stream) {
+  float* part = nullptr;
+  uint32_t* cnt = nullptr;
+  if (cudaMalloc(&part, kTailPartialBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  ++g_alloc_count;
+  if (cudaMalloc(&cnt, kTailFlagWords * sizeof(uint32_t)) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(part);
+    return false;
+  }
+  ++g_alloc_count;
+  if (cudaMemsetAsync(cnt, 0, kTailFlagWords * sizeof(uint32_t), stream) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(part);
+    cudaFree(cnt);
+    return false;
+  }
+  t.partials = part;
+  t.counters = cnt;
+  return true;
+}
+
+// Grows the workspace of `t` to at least `bytes` (synchronising `stream`
+// first when an older, smaller buffer may still be in use).  Caller holds
+// g_mutex.
+int grow_workspace(StreamState& t, size_t bytes, cudaStream_t stream) {
+  if (t.ws) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaFree(t.ws);
+    t.ws = nullptr;
+    t.ws_bytes = 0;
+  }
+  const size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, want);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ++g_alloc_count;
+  t.ws = p;
+  t.ws_bytes = want;
+  return TG_OK;
+}
+
 }  // namespace
 
-bool tail_scratch(cudaStream_t stream, float** partials, uint32_t** flags) {
+bool tail_scratch(cudaStream_t stream, float** partials, uint32_t** counters) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  std::lock_guard<std::mutex> lk(g_mutex);
-  const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
-  auto it = g_tail.find(key);
-  if (it == g_tail.end()) {
-    TailScratch t;
-    if (cudaMalloc(&t.partials, kTailPartialBytes) != cudaSuccess) {
-      cudaGetLastError();
-      return false;
-    }
-    if (cudaMalloc(&t.flags, kTailFlagWords * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(t.flags, 0, kTailFlagWords * sizeof(uint32_t)) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFree(t.partials);
-      if (t.flags) cudaFree(t.flags);
-      return false;
-    }
-    it = g_tail.emplace(key, t).first;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
   }
-  *partials = it->second.partials;
-  *flags = it->second.flags;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  StreamState& t = g_streams[stream_key(dev, stream)];
+  if (t.partials == nullptr) {
+    // Without a reservation the scratch is allocated on first need, except
+    // while the stream is captured (the product then runs unsplit).
+    if (t.reserved || stream_capturing(stream) || !alloc_tail_scratch(t, stream)) return false;
+  }
+  *partials = t.partials;
+  *counters = t.counters;
   return true;
 }
 
@@ -200,38 +263,74 @@ void reset_tail_flags() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return;
   std::lock_guard<std::mutex> lk(g_mutex);
-  for (auto& kv : g_tail)
-    if (kv.first.first == dev) cudaMemset(kv.second.flags, 0, kTailFlagWords * sizeof(uint32_t));
+  for (auto& kv : g_streams)
+    if (kv.first.first == dev && kv.second.counters)
+      cudaMemset(kv.second.counters, 0, kTailFlagWords * sizeof(uint32_t));
 }
 
-void* device_workspace(size_t bytes, cudaStream_t stream) {
+void* device_workspace(size_t bytes, cudaStream_t stream, int* rc) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mutex);
-  Workspace& w = g_workspace[std::make_pair(dev, reinterpret_cast<uintptr_t>(stream))];
-  if (w.bytes >= bytes && w.ptr) return w.ptr;
-  if (w.ptr) {
-    // Earlier work on this stream may still read the old buffer (a stream
-    // being captured cannot be synchronised: the call fails).
-    cudaError_t e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) {
-      cuda_fail(e);
-      return nullptr;
-    }
-    cudaFree(w.ptr);
-    w.ptr = nullptr;
-    w.bytes = 0;
-  }
-  size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
-  void* p = nullptr;
-  cudaError_t e = cudaMalloc(&p, want);
-  if (e != cudaSuccess) {
-    cuda_fail(e);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *rc = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
     return nullptr;
   }
-  w.ptr = p;
-  w.bytes = want;
-  return p;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  StreamState& t = g_streams[stream_key(dev, stream)];
+  if (t.ws && t.ws_bytes >= bytes) return t.ws;
+  if (t.reserved || stream_capturing(stream)) {
+    *rc = TG_ERR_WORKSPACE;
+    return nullptr;
+  }
+  *rc = grow_workspace(t, bytes, stream);
+  return *rc == TG_OK ? t.ws : nullptr;
+}
+
+int reserve_workspace(cudaStream_t stream, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (stream_capturing(stream)) return TG_ERR_WORKSPACE;
+  StreamState& t = g_streams[stream_key(dev, stream)];
+  if (!t.ws || t.ws_bytes < bytes) {
+    const int rc = grow_workspace(t, bytes, stream);
+    if (rc != TG_OK) return rc;
+  }
+  if (t.partials == nullptr && !alloc_tail_scratch(t, stream)) return cuda_fail(cudaErrorMemoryAllocation);
+  // The counters' zeroing (and any earlier use of a replaced buffer) is
+  // complete before the reservation is reported.
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t.reserved = true;
+  return TG_OK;
+}
+
+uint64_t alloc_count() {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  return g_alloc_count;
+}
+
+bool device_local(const void* ptr, int dev) {
+  if (ptr == nullptr) return false;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+bool operands_local(const void* const* ptrs, int n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  for (int i = 0; i < n; ++i)
+    if (!device_local(ptrs[i], dev)) return false;
+  return true;
 }
 
 int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,
@@ -240,12 +339,14 @@ int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb
                 unsigned flags, cudaStream_t stream, DeviceCtx* ctx) {
   if (K == 0) return launch_fill_epilogue(D, ldd, M, N, d_dtype, epi, stream);
   const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
-  const bool mcast = (flags & TG_FLAG_MULTICAST) != 0;
+  const bool mcast_flag = (flags & TG_FLAG_MULTICAST) != 0;
+  int rc = TG_OK;
   if (kind == kKindBf16) {
+    const bool mcast = bf16_uses_multicast(A, B, M, N, K, pair, mcast_flag);
     const Bf16Repitch rp = bf16_repitch_plan(lda, ldb, M, N, K);
     if (rp.bytes != 0) {
-      void* ws = device_workspace(rp.bytes, stream);
-      if (ws == nullptr) return TG_ERR_CUDA;
+      void* ws = device_workspace(rp.bytes, stream, &rc);
+      if (ws == nullptr) return rc;
       return launch_gemm_bf16_repitched(rp, A, lda, B, ldb, D, ldd, static_cast<int>(M),
                                         static_cast<int>(N), static_cast<int>(K), d_dtype, epi,
                                         pair, mcast, ws, stream, ctx);
@@ -254,9 +355,13 @@ int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb
                                  static_cast<int>(N), static_cast<int>(K), d_dtype, epi, pair,
                                  mcast, stream, ctx);
   }
+  // Block-scaled multicast clusters (MXFP8 pairs) load B by TMA multicast:
+  // only over memory of the current device.
+  const void* ops[4] = {A, B, SFA, SFB};
+  const bool mcast = mcast_flag && operands_local(ops, 4);
   uint8_t* ws = static_cast<uint8_t*>(
-      device_workspace(blockscaled_workspace_bytes(kind, M, N, K, pair), stream));
-  if (ws == nullptr) return TG_ERR_CUDA;
+      device_workspace(blockscaled_workspace_bytes(kind, M, N, K, pair), stream, &rc));
+  if (ws == nullptr) return rc;
   return launch_gemm_blockscaled_impl(kind, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
                                       static_cast<int>(M), static_cast<int>(N),
                                       static_cast<int>(K), d_dtype, epi, pair, mcast, ws,
@@ -431,8 +536,8 @@ int gemm_bf16_skinny(const void* A, int64_t lda, const void* B, int64_t ldb, voi
   float* ws = nullptr;
   const size_t ws_bytes = skinny_workspace_bytes(M, N, d_dtype, e.op);
   if (ws_bytes) {
-    ws = static_cast<float*>(device_workspace(ws_bytes, stream));
-    if (ws == nullptr) return TG_ERR_CUDA;
+    ws = static_cast<float*>(device_workspace(ws_bytes, stream, &rc));
+    if (ws == nullptr) return rc;
   }
   return launch_gemm_skinny_impl(A, lda, B, ldb, D, ldd, static_cast<int>(M), static_cast<int>(N),
                                  static_cast<int>(K), d_dtype, e, split_k, ws, stream, ctx);
@@ -463,8 +568,8 @@ int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* 
     return launch_gemm_bf16_gather_impl(A, lda, static_cast<int>(a_rows), row_idx,
                                         static_cast<int>(M), B, ldb, D, ldd, static_cast<int>(N),
                                         static_cast<int>(K), d_dtype, e, pair, stream, ctx);
-  void* ws = device_workspace(gather_workspace_bytes(M, K), stream);
-  if (ws == nullptr) return TG_ERR_CUDA;
+  void* ws = device_workspace(gather_workspace_bytes(M, K), stream, &rc);
+  if (ws == nullptr) return rc;
   return launch_gemm_bf16_pregather_impl(A, lda, static_cast<int>(a_rows), row_idx,
                                          static_cast<int>(M), B, ldb, D, ldd, static_cast<int>(N),
                                          static_cast<int>(K), d_dtype, e, pair, ws, stream, ctx);
@@ -478,6 +583,57 @@ int tg_gemm_tail_split(int64_t M, int64_t N, int64_t K, unsigned flags) {
   if (!ctx) return -TG_ERR_CUDA;
   return bf16_tail_split(M, N, K, (flags & TG_FLAG_CTA_PAIR) != 0, ctx);
 }
+
+int tg_gemm_multicast(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                      unsigned flags) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return -TG_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST))
+    return -TG_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0 || K == 0) return 0;   // nothing, or the K = 0 fill, runs
+  return bf16_uses_multicast(A, B, M, N, K, (flags & TG_FLAG_CTA_PAIR) != 0,
+                             (flags & TG_FLAG_MULTICAST) != 0)
+             ? 1
+             : 0;
+}
+
+int64_t tg_workspace_bytes(int call, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                           int d_dtype, int epi_op, unsigned flags) {
+  if (M < 0 || N < 0 || K < 0 || lda < 0 || ldb < 0 || M > kMaxDim || N > kMaxDim ||
+      K > kMaxDim)
+    return -TG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0 || K == 0) return 0;
+  const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
+  switch (call) {
+    case TG_CALL_GEMM_BF16:
+      return static_cast<int64_t>(bf16_repitch_plan(lda, ldb, M, N, K).bytes);
+    case TG_CALL_GEMM_MXFP8:
+      if (K % 32) return -TG_ERR_INVALID_ARG;
+      return static_cast<int64_t>(blockscaled_workspace_bytes(kKindMxf8, M, N, K, pair));
+    case TG_CALL_GEMM_MXFP4:
+      if (K % 32) return -TG_ERR_INVALID_ARG;
+      return static_cast<int64_t>(blockscaled_workspace_bytes(kKindMxf4, M, N, K, pair));
+    case TG_CALL_GEMM_NVFP4:
+      if (K % 16) return -TG_ERR_INVALID_ARG;
+      return static_cast<int64_t>(blockscaled_workspace_bytes(kKindNvf4, M, N, K, pair));
+    case TG_CALL_GEMM_BF16_SKINNY:
+      if (M > 128) return -TG_ERR_UNSUPPORTED;
+      if (d_dtype != TG_D_F32 && d_dtype != TG_D_BF16) return -TG_ERR_INVALID_ARG;
+      if (epi_op < kEpiNone || epi_op > kEpiAffine) return -TG_ERR_INVALID_ARG;
+      return static_cast<int64_t>(skinny_workspace_bytes(M, N, d_dtype, epi_op));
+    case TG_CALL_GEMM_BF16_GATHER:
+      return (flags & TG_FLAG_GATHER_TMA) ? 0 : static_cast<int64_t>(gather_workspace_bytes(M, K));
+    default:
+      return -TG_ERR_INVALID_ARG;
+  }
+}
+
+int tg_reserve_workspace(void* cuda_stream, int64_t bytes) {
+  if (bytes < 0) return TG_ERR_INVALID_ARG;
+  return reserve_workspace(as_stream(cuda_stream), static_cast<size_t>(bytes));
+}
+
+uint64_t tg_workspace_alloc_count(void) { return alloc_count(); }
 
 int tg_gemm_repitch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
   if (M < 0 || N < 0 || K < 0 || lda < 0 || ldb < 0) return -TG_ERR_INVALID_ARG;
@@ -560,12 +716,14 @@ const char* tg_status_string(int status) {
     case TG_ERR_CUDA: return "CUDA error";
     case TG_ERR_TIMEOUT: return "device pipeline wait timed out";
     case TG_ERR_NO_SCRATCH: return "problem needs more scratch than the static no-allocation buffer";
+    case TG_ERR_WORKSPACE:
+      return "the stream's workspace is too small and may not grow now (reserved, or the stream is being captured)";
     default: return "unknown status";
   }
 }
 
 int tg_last_cuda_error(void) { return t_last_cuda_error; }
 
-int tg_version(void) { return 100; }
+int tg_version(void) { return 200; }
 
 }  // extern "C"

@@ -32,11 +32,22 @@ bool single_cta_multicast_pays(int64_t M, int64_t N, int64_t K) {
   return K <= 1536 && M >= 3000 && N >= 3000;
 }
 
+// Multicast clusters, asked for (TG_FLAG_MULTICAST) or chosen for short K,
+// load the shared B tile with .multicast::cluster TMA.  They run only when A
+// and B are allocations of the current device, so that a multicast tensor map
+// never covers another GPU's (or the host's) memory; otherwise the plain
+// pair or single-CTA kernel computes the same result.
+bool bf16_uses_multicast(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                         bool pair, bool mcast_flag) {
+  if (!mcast_flag && (pair || !single_cta_multicast_pays(M, N, K))) return false;
+  const void* ops[2] = {A, B};
+  return operands_local(ops, 2);
+}
+
 int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb, void* D,
                           int64_t ldd, int M, int N, int K, int d_dtype, const Epi& epi,
                           bool pair, bool mcast, cudaStream_t stream, DeviceCtx* ctx) {
   constexpr int BN = 256;
-  if (!pair && !mcast && single_cta_multicast_pays(M, N, K)) mcast = true;
   const int g = pair ? 2 : 1;
   const int b_rows = BN / g;
   CUtensorMap tA, tB;
@@ -80,7 +91,9 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
 }
 
 int bf16_tail_split(int64_t M, int64_t N, int64_t K, bool pair, DeviceCtx* ctx) {
-  if (!pair && single_cta_multicast_pays(M, N, K)) return 1;   // clusters never split
+  // Clusters never split (operands in this device's memory pick them for
+  // short K).
+  if (!pair && single_cta_multicast_pays(M, N, K)) return 1;
   const int g = pair ? 2 : 1;
   const int num_tiles = ceil_div_i(M, 128 * g) * ceil_div_i(N, 256);
   const int units_max =

@@ -140,7 +140,8 @@ int launch_gemm_blockscaled_impl(int kind, const void* A, int64_t lda, const voi
                                  int64_t ldb, const void* SFA, int64_t ld_sfa, const void* SFB,
                                  int64_t ld_sfb, void* D, int64_t ldd, int M, int N, int K,
                                  int d_dtype, const Epi& epi, bool pair, bool mcast,
-                                 uint8_t* sf_workspace, cudaStream_t stream, DeviceCtx* ctx) {
+                                 uint8_t* sf_workspace, cudaStream_t stream, DeviceCtx* ctx,
+                                 bool no_scratch) {
   const BsPlan pl = plan_bs(kind, M, N, K, pair);
   const int g = pair ? 2 : 1;
   uint8_t* img_a = sf_workspace;
@@ -201,6 +202,7 @@ int launch_gemm_blockscaled_impl(int kind, const void* A, int64_t lda, const voi
   a.raster_group = kRasterGroup;
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
+  a.no_scratch = no_scratch;
   const bool bf16_out = d_dtype == TG_D_BF16;
   if (kind != kKindMxf8)
     return launch_gemm_fp4_cfg(kind, pair, bf16_out, tA, tB, tSA, tSB, a, stream, ctx);
@@ -218,10 +220,10 @@ int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ld
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int M, int N, int K, int d_dtype,
                            const Epi& epi, bool pair, bool mcast, uint8_t* sf_workspace,
-                           cudaStream_t stream, DeviceCtx* ctx) {
+                           cudaStream_t stream, DeviceCtx* ctx, bool no_scratch) {
   return launch_gemm_blockscaled_impl(kKindMxf8, A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D,
                                       ldd, M, N, K, d_dtype, epi, pair, mcast, sf_workspace,
-                                      stream, ctx);
+                                      stream, ctx, no_scratch);
 }
 
 }  // namespace tg

@@ -73,7 +73,10 @@ int launch_gemm_bf16_pregather_impl(const void* A, int64_t lda, int a_rows, cons
       static_cast<uint16_t*>(workspace), ldg, K);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
-  return launch_gemm_bf16_impl(workspace, ldg, B, ldb, D, ldd, M, N, K, d_dtype, epi, pair, false,
+  // The gathered rows live in this device's workspace; B decides whether the
+  // short-K multicast clusters may run.
+  const bool mcast = bf16_uses_multicast(workspace, B, M, N, K, pair, false);
+  return launch_gemm_bf16_impl(workspace, ldg, B, ldb, D, ldd, M, N, K, d_dtype, epi, pair, mcast,
                                stream, ctx);
 }
 

@@ -56,7 +56,6 @@ enum : uint32_t {
   kSiteMmaAccEmpty = 3,
   kSiteEpiAccFull = 4,
   kSiteScaleFull = 5,
-  kSiteTailFlag = 6,
 };
 
 struct GemmArgs {
@@ -74,17 +73,22 @@ struct GemmArgs {
   int gather_rows;        // rows of A; indices outside [0, gather_rows) read zeros
   // Tail split (see next_work): tiles below full_tiles are whole work items;
   // with tail_split = S > 1 the tail_items = R * S items that follow are K
-  // pieces of the R last tiles.  Piece p > 0 writes its f32 partial tile to
-  // partials and sets its flag to 1; piece 0 waits for the flags, adds the
-  // partials before its epilogue and sets the flags back to 0, so that every
-  // launch (also a graph replay) starts from zeroed flags.
+  // pieces of the R last tiles.  Every epilogue warp of every piece writes
+  // its share of the piece's f32 partial tile to partials and then arrives on
+  // its share's counter; the arrival that completes the count (the S-th)
+  // adds the S partials in piece order, stores D and sets the counter back
+  // to 0, so that every launch (also a graph replay) starts from zeroed
+  // counters.  No piece waits for another.
   int full_tiles;
   int tail_split;
   int tail_items;
-  float* partials;        // [tail tile][piece-1][CTA of pair][BN cols][128 rows] f32
-  uint32_t* flags;        // [tail tile][piece-1][CTA of pair], 0 between launches
+  float* partials;        // [tail tile][piece][CTA of pair][BN cols][128 rows] f32
+  uint32_t* counters;     // [tail tile][CTA of pair][epilogue warp], 0 between launches
   uint32_t* status;
   uint64_t timeout_ns;
+  // Host side only (the kernel ignores it): the call must not allocate, so
+  // the launcher never turns on the tail split, whose scratch is allocated.
+  bool no_scratch;
 };
 
 // kKind_: kKindBf16 (dense bf16) or one of the block-scaled kinds kKindMxf8,
@@ -200,16 +204,17 @@ struct Work {
   int t;        // tile id (tile order)
   int k0, k1;   // K stages k0, k0 + ks, ... below k1
   int ks;
-  int piece;    // K piece (0: the owner, which stores D)
+  int piece;    // K piece (its partial's slot; the order in which partials add up)
   int tail;     // tail tile index, or -1 for a whole tile
 };
 
 // Item i of `unit`: tiles unit, unit + U, ... below full_tiles; then, with a
 // tail split, the unit's one K piece of a tail tile.  Every unit runs full
 // waves of whole tiles (full_tiles = W * U), and the R tiles a last, partial
-// wave would leave to R units are cut into S pieces run by R * S units at
-// once.  All units of the grid are resident together, and only owners wait
-// (for pieces that never wait), so the pieces cannot block each other.
+// wave would leave to R units are cut into S pieces run by R * S units.  The
+// pieces never wait for each other: the last one to finish adds the partial
+// tiles and stores D, so the result does not depend on which units of the
+// grid are resident at the same time.
 __device__ __forceinline__ bool next_work(const GemmArgs& p, int unit, int num_units, int i,
                                           Work& w) {
   const int t = unit + i * num_units;
@@ -458,9 +463,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t* sf_drain_bar = sfr_bar + C::kStages;      // [kSfWarps] copies on give-up
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  // Tail split: epilogue warps done with their piece / done waiting as owner.
-  int* tail_count = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
-  int* owner_count = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
@@ -493,8 +495,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int w = 0; w < C::kSfWarps; ++w) mbar_init(&sf_drain_bar[w], 1);
     }
     *abort_flag = 0;
-    *tail_count = 0;
-    *owner_count = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -883,21 +883,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(slab * 32) << 16) +
                              static_cast<uint32_t>(acc * C::ACC_COLS + half * C::kEpiCols);
-      // Tail split.  A partial tile is stored column-major, [BN][128] f32:
-      // the 32 lanes of a warp (32 consecutive rows) then write and read 128
-      // contiguous bytes per column.  part_col(q) points at this thread's row
-      // in the first of its columns; flag_of(q) is piece q's ready flag.
-      const int S1 = p.tail_split - 1;
-      auto part_col = [&](int piece) {
-        return p.partials +
-               ((static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup + pair_rank) *
-                   (128 * C::BN) +
-               static_cast<int64_t>(half * C::kEpiCols) * 128 + row_in_tile;
-      };
-      auto flag_of = [&](int piece) {
-        return p.flags + (static_cast<int64_t>(w.tail) * S1 + (piece - 1)) * C::kCtaGroup +
-               pair_rank;
-      };
       if constexpr (C::kTmaStore && C::kAccBufs == 2) {
         // Box-wise: the accumulator is read one box (32 rows x 128 bytes of
         // D) at a time, which keeps 32 or 64 values live instead of 128; the
@@ -905,114 +890,141 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // The buffer goes back after its last read.
         constexpr int kPerBox = C::kBf16Out ? 2 : 1;   // accumulator chunks per box
         constexpr int kBoxes = C::kEpiChunks / kPerBox;
-        const bool tail_piece = w.tail >= 0 && w.piece > 0;
-        const bool tail_owner = w.tail >= 0 && w.piece == 0;
-        if (tail_owner) {
-          int ready = 1;
-          if (lane == 0)
-            for (int q = 1; q <= S1 && ready; ++q)
-              ready = flag_wait_eq(flag_of(q), 1u, guard, kSiteTailFlag) ? 1 : 0;
-          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
-          if (!ready) break;
-          for (int q = 1; q <= S1; ++q) {
-            uint32_t seen;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
-                         : "=r"(seen)
-                         : "l"(flag_of(q))
-                         : "memory");
-            (void)seen;
-          }
-        }
         const int row0 = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + slab * 32;
         const int col_base = tn * C::BN + half * C::kEpiCols;
+        // Tail split.  A partial tile is stored column-major, [BN][128] f32:
+        // the 32 lanes of a warp (32 consecutive rows) then write and read 128
+        // contiguous bytes per column.  part_col(q) points at this thread's
+        // row in the first of its columns in piece q's partial.
+        const int S = p.tail_split;
+        auto part_col = [&](int piece) {
+          return p.partials +
+                 ((static_cast<int64_t>(w.tail) * S + piece) * C::kCtaGroup + pair_rank) *
+                     (128 * C::BN) +
+                 static_cast<int64_t>(half * C::kEpiCols) * 128 + row_in_tile;
+        };
+        bool store_d = true;
+        if (w.tail >= 0) {
+          // Publish this piece's share of the partial tile, then arrive on
+          // the share's counter (one per epilogue warp of each CTA).
+          float* dst = part_col(w.piece);
 #pragma unroll
-        for (int b = 0; b < kBoxes; ++b) {
-          uint32_t vb[kPerBox][32];
+          for (int b = 0; b < kBoxes; ++b) {
+            uint32_t vb[kPerBox][32];
 #pragma unroll
-          for (int h = 0; h < kPerBox; ++h)
-            tmem_ld_32x32b_x32(t_row + 32 * (kPerBox * b + h), vb[h]);
-          tmem_ld_wait();
-          if (b == kBoxes - 1) {
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (C::kCtaGroup == 1)
-                mbar_arrive_relaxed(&acce_bar[acc]);
-              else
-                mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+            for (int h = 0; h < kPerBox; ++h)
+              tmem_ld_32x32b_x32(t_row + 32 * (kPerBox * b + h), vb[h]);
+            tmem_ld_wait();
+            if (b == kBoxes - 1) {
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) {
+                if constexpr (C::kCtaGroup == 1)
+                  mbar_arrive_relaxed(&acce_bar[acc]);
+                else
+                  mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+              }
             }
-          }
-          if (tail_piece) {
-            float* dst = part_col(w.piece);
 #pragma unroll
             for (int h = 0; h < kPerBox; ++h)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 __stcg(dst + (32 * (kPerBox * b + h) + i) * 128, __uint_as_float(vb[h][i]));
-            continue;
           }
-          if (tail_owner)
-            for (int q = 1; q <= S1; ++q) {
-              const float* src = part_col(q);
+          // Every lane's partial stores are ordered before lane 0's arrival.
+          __threadfence();
+          __syncwarp();
+          uint32_t* counter =
+              p.counters + (static_cast<int64_t>(w.tail) * C::kCtaGroup + pair_rank) * C::kEpiWarps +
+              (warp - 2);
+          uint32_t prev = 0;
+          if (lane == 0) prev = arrive_counter_gpu(counter);
+          prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+          store_d = prev == static_cast<uint32_t>(S - 1);
+          if (store_d) {
+            // The last arrival: every other piece's share is published.
+            // Nobody touches the counter again in this launch.
+            __threadfence();
+            if (lane == 0) *counter = 0u;
+          }
+        }
+        if (store_d) {
+#pragma unroll
+          for (int b = 0; b < kBoxes; ++b) {
+            uint32_t vb[kPerBox][32];
+            if (w.tail < 0) {
+#pragma unroll
+              for (int h = 0; h < kPerBox; ++h)
+                tmem_ld_32x32b_x32(t_row + 32 * (kPerBox * b + h), vb[h]);
+              tmem_ld_wait();
+              if (b == kBoxes - 1) {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                  if constexpr (C::kCtaGroup == 1)
+                    mbar_arrive_relaxed(&acce_bar[acc]);
+                  else
+                    mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
+                }
+              }
+            } else {
+              // The pieces' partials, added in piece order 0, 1, ..., S-1
+              // whichever piece arrived last, so repeated calls give the
+              // same bits.
+              const float* src0 = part_col(0);
 #pragma unroll
               for (int h = 0; h < kPerBox; ++h)
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                  vb[h][i] = __float_as_uint(__uint_as_float(vb[h][i]) +
-                                             __ldcg(src + (32 * (kPerBox * b + h) + i) * 128));
-            }
-          const int col0 = col_base + 32 * kPerBox * b;
-          if (row0 < p.M && col0 < p.N) {
-            if (!epi_lean) {
+                  vb[h][i] = __float_as_uint(__ldcg(src0 + (32 * (kPerBox * b + h) + i) * 128));
+              for (int q = 1; q < S; ++q) {
+                const float* src = part_col(q);
 #pragma unroll
-              for (int h = 0; h < kPerBox; ++h)
-                if (col0 + 32 * h < p.N) epilogue_general_chunk(p, col0 + 32 * h, vb[h]);
-            }
-            if (col0 + 32 * kPerBox <= p.N) {
-              // The previous box's store has finished reading the buffer.
-              if (lane == 0) bulk_wait_group_read0();
-              __syncwarp();
-              if (epi_lean)
-                epilogue_stage_box<C, true>(stg_row, lane, vb[0], vb[kPerBox - 1], epi_add);
-              else
-                epilogue_stage_box<C, false>(stg_row, lane, vb[0], vb[kPerBox - 1], 0.0f);
-              fence_proxy_async_smem();
-              __syncwarp();
-              // Rows >= M are clipped by the store.
-              if (lane == 0) {
-                tma_store_2d_hint(&tmD, stg, col0, row0, pol_d);
-                bulk_commit_group();
+                for (int h = 0; h < kPerBox; ++h)
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    vb[h][i] = __float_as_uint(__uint_as_float(vb[h][i]) +
+                                               __ldcg(src + (32 * (kPerBox * b + h) + i) * 128));
               }
-            } else {
-              // The box crosses column N: a clipped TMA store may write up to
-              // the next 16-byte boundary past N, into the caller's row
-              // padding, so the ragged box is stored from registers.
-              const int row = row0 + static_cast<int>(lane);
+            }
+            const int col0 = col_base + 32 * kPerBox * b;
+            if (row0 < p.M && col0 < p.N) {
+              if (!epi_lean) {
 #pragma unroll
-              for (int h = 0; h < kPerBox; ++h)
-                if (row < p.M && col0 + 32 * h < p.N) {
-                  if (epi_lean)
-                    epilogue_store_chunk<C, true>(p, row, col0 + 32 * h, vb[h], epi_add, pol_d);
-                  else
-                    epilogue_store_chunk<C, false>(p, row, col0 + 32 * h, vb[h], 0.0f, pol_d);
+                for (int h = 0; h < kPerBox; ++h)
+                  if (col0 + 32 * h < p.N) epilogue_general_chunk(p, col0 + 32 * h, vb[h]);
+              }
+              if (col0 + 32 * kPerBox <= p.N) {
+                // The previous box's store has finished reading the buffer.
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+                if (epi_lean)
+                  epilogue_stage_box<C, true>(stg_row, lane, vb[0], vb[kPerBox - 1], epi_add);
+                else
+                  epilogue_stage_box<C, false>(stg_row, lane, vb[0], vb[kPerBox - 1], 0.0f);
+                fence_proxy_async_smem();
+                __syncwarp();
+                // Rows >= M are clipped by the store.
+                if (lane == 0) {
+                  tma_store_2d_hint(&tmD, stg, col0, row0, pol_d);
+                  bulk_commit_group();
                 }
+              } else {
+                // The box crosses column N: a clipped TMA store may write up to
+                // the next 16-byte boundary past N, into the caller's row
+                // padding, so the ragged box is stored from registers.
+                const int row = row0 + static_cast<int>(lane);
+#pragma unroll
+                for (int h = 0; h < kPerBox; ++h)
+                  if (row < p.M && col0 + 32 * h < p.N) {
+                    if (epi_lean)
+                      epilogue_store_chunk<C, true>(p, row, col0 + 32 * h, vb[h], epi_add, pol_d);
+                    else
+                      epilogue_store_chunk<C, false>(p, row, col0 + 32 * h, vb[h], 0.0f, pol_d);
+                  }
+              }
             }
           }
-        }
-        if (tail_piece) {
-          // Publish the partial: the last epilogue warp to finish sets the flag.
-          __threadfence();
-          __syncwarp();
-          if (lane == 0 && atomicAdd(tail_count, 1) == C::kEpiWarps - 1) {
-            __threadfence();
-            flag_set_release(flag_of(w.piece), 1u);
-          }
-        } else if (tail_owner) {
-          // Once all eight epilogue warps have seen the flags, the last one
-          // sets them back to 0 for the next launch.
-          __syncwarp();
-          if (lane == 0 && atomicAdd(owner_count, 1) == C::kEpiWarps - 1)
-            for (int q = 1; q <= S1; ++q) flag_set_release(flag_of(q), 0u);
         }
       } else {
         // Read this warp's whole share of the accumulator, then hand the
@@ -1030,56 +1042,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             mbar_arrive_relaxed(&acce_bar[acc]);
           else
             mbar_arrive_relaxed_cluster(acce_remote + 8u * static_cast<uint32_t>(acc));
-        }
-        if (w.tail >= 0) {
-          if (w.piece > 0) {
-            // A K piece: publish the raw f32 partial for the owner, store no D.
-            float* dst = part_col(w.piece);
-#pragma unroll
-            for (int c = 0; c < C::kEpiChunks; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                __stcg(dst + (32 * c + i) * 128, __uint_as_float(v[c][i]));
-            __threadfence();
-            __syncwarp();
-            // The last of the epilogue warps to finish releases the flag.
-            if (lane == 0 && atomicAdd(tail_count, 1) == C::kEpiWarps - 1) {
-              __threadfence();
-              flag_set_release(flag_of(w.piece), 1u);
-            }
-            if (++acc == C::kAccBufs) {
-              acc = 0;
-              acc_phase ^= 1u;
-            }
-            continue;
-          }
-          // The owner: wait for every other piece (bounded), then add them.
-          int ready = 1;
-          if (lane == 0)
-            for (int q = 1; q <= S1 && ready; ++q)
-              ready = flag_wait_eq(flag_of(q), 1u, guard, kSiteTailFlag) ? 1 : 0;
-          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
-          if (!ready) break;
-          for (int q = 1; q <= S1; ++q) {
-            uint32_t seen;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
-                         : "=r"(seen)
-                         : "l"(flag_of(q))
-                         : "memory");
-            (void)seen;
-            const float* src = part_col(q);
-#pragma unroll
-            for (int c = 0; c < C::kEpiChunks; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                v[c][i] = __float_as_uint(__uint_as_float(v[c][i]) +
-                                          __ldcg(src + (32 * c + i) * 128));
-          }
-          // Once all eight epilogue warps have seen the flags, the last one
-          // sets them back to 0 for the next launch.
-          __syncwarp();
-          if (lane == 0 && atomicAdd(owner_count, 1) == C::kEpiWarps - 1)
-            for (int q = 1; q <= S1; ++q) flag_set_release(flag_of(q), 0u);
         }
         const int row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM + row_in_tile;
         const int col_base = tn * C::BN + half * C::kEpiCols;

@@ -63,13 +63,16 @@ int tail_split_for(int num_tiles, int num_k_blocks, int units_max, int* W, int* 
   // 8192 in pairs: 45 -> 39 us; after full waves 4096^3 93.5 -> 90.4 us,
   // 8192^3 in pairs 654 -> 640 us).  For the block-scaled kinds the exchange
   // of partial tiles cost more than it saved (1024 x 1024 x 8192 MXFP8:
-  // 29 -> 33 us).  So: dense kinds only.
-  if (C::kMcast || C::kMx || *R == 0 || 2 * *R > units_max) return 1;
+  // 29 -> 33 us).  So: dense kinds only, and only the configurations whose
+  // epilogue does the exchange (two accumulators, box-wise TMA stores).
+  if (C::kMcast || C::kMx || !C::kTmaStore || C::kAccBufs != 2) return 1;
+  if (*R == 0 || 2 * *R > units_max) return 1;
   int S = units_max / *R;
   if (S > 4) S = 4;
   while (S >= 2 && num_k_blocks < 4 * S) --S;
-  const size_t bytes = static_cast<size_t>(*R) * (S - 1) * C::kCtaGroup * 128 * C::BN * 4;
-  if (S < 2 || bytes > kTailPartialBytes || *R * (S - 1) * C::kCtaGroup > kTailFlagWords)
+  // Every piece publishes its partial tile; one counter per epilogue warp.
+  const size_t bytes = static_cast<size_t>(*R) * S * C::kCtaGroup * 128 * C::BN * 4;
+  if (S < 2 || bytes > kTailPartialBytes || *R * C::kCtaGroup * C::kEpiWarps > kTailFlagWords)
     return 1;
   return S;
 }
@@ -87,21 +90,22 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
   a.tail_split = 1;
   a.tail_items = 0;
   a.partials = nullptr;
-  a.flags = nullptr;
-  {
+  a.counters = nullptr;
+  if (!args.no_scratch) {
     // Tail split: W full waves of whole tiles over all units; the R tiles of
     // a last, partial wave are cut into S K-pieces (S <= units / R, at most
     // 4, each piece at least 4 stages) so that R * S units finish together.
+    // Calls that must not allocate (no_scratch) never split.
     int W = 0, R = 0;
     const int S = tail_split_for<C>(num_tiles, args.num_k_blocks, units_max, &W, &R);
     float* part = nullptr;
-    uint32_t* flags = nullptr;
-    if (S >= 2 && tail_scratch(stream, &part, &flags)) {
+    uint32_t* counters = nullptr;
+    if (S >= 2 && tail_scratch(stream, &part, &counters)) {
       a.full_tiles = W * units_max;
       a.tail_split = S;
       a.tail_items = R * S;
       a.partials = part;
-      a.flags = flags;
+      a.counters = counters;
       units = W > 0 ? units_max : R * S;
     }
   }

@@ -96,8 +96,12 @@ extern "C" int gemm_mxfp8_blockscaled_noalloc(const void* A, int64_t lda, const 
   if (!ctx) return TG_ERR_CUDA;
   uint8_t* scratch = noalloc_scratch(&rc);
   if (scratch == nullptr) return rc;
+  // Multicast clusters only over operands in this device's memory.
+  const void* ops[4] = {A, B, SFA, SFB};
+  const bool mcast = (flags & TG_FLAG_MULTICAST) != 0 && operands_local(ops, 4);
+  // no_scratch: the launcher must not turn on anything that allocates.
   return launch_gemm_mxfp8_impl(A, lda, B, ldb, SFA, ld_sfa, SFB, ld_sfb, D, ldd,
                                 static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                d_dtype, epi, pair, (flags & TG_FLAG_MULTICAST) != 0, scratch,
-                                stream, ctx);
+                                d_dtype, epi, pair, mcast, scratch, stream, ctx,
+                                /*no_scratch=*/true);
 }

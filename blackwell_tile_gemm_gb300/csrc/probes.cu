@@ -431,6 +431,19 @@ __global__ void wait_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
   }
 }
 
+// ------------------------------------------------------------- SM occupier
+// One warp per block with enough dynamic shared memory that no GEMM CTA fits
+// beside it on the SM; it sleeps until `ns` have passed on the global timer.
+// The loop is bounded by an iteration count as well as by the timer.
+__global__ void hold_sms_kernel(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  const uint64_t max_iters = ns / 256u + 1024u;
+  for (uint64_t i = 0; i < max_iters; ++i) {
+    if (global_timer_ns() - t0 >= ns) break;
+    __nanosleep(1000);
+  }
+}
+
 }  // namespace
 }  // namespace tg
 
@@ -581,6 +594,16 @@ int tg_probe_mma_rate(int kind, int iters, int ctas, unsigned long long* cycles,
       mma_rate_kernel<4><<<ctas, 128, smem, st>>>(iters, cycles, ctx->status, wait_timeout_ns());
   }
   if (e != cudaSuccess) return cuda_fail(e);
+  return launched();
+}
+
+int tg_probe_hold_sms(int blocks, uint64_t ns, void* s) {
+  if (blocks < 1 || blocks > 4096 || ns == 0 || ns > 1000000000ull) return TG_ERR_INVALID_ARG;
+  const int smem = 200 * 1024;
+  cudaError_t e =
+      cudaFuncSetAttribute(hold_sms_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  hold_sms_kernel<<<blocks, 32, smem, static_cast<cudaStream_t>(s)>>>(ns);
   return launched();
 }
 

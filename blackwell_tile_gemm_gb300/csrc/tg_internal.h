@@ -36,23 +36,40 @@ int make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
                        uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
 // Library-owned device workspace for (current device, `stream`), at least
-// `bytes` long (grown on demand: growing synchronises the stream first, so
-// make the largest call on a stream before capturing it into a graph).
-// nullptr on failure.
-void* device_workspace(size_t bytes, cudaStream_t stream);
+// `bytes` long.  Without a reservation it is grown on demand (growing
+// synchronises the stream first); a reserved workspace never grows.  When it
+// is too small and cannot grow (reserved, or the stream is being captured)
+// *rc = TG_ERR_WORKSPACE; on a CUDA failure *rc = TG_ERR_CUDA.  nullptr then.
+void* device_workspace(size_t bytes, cudaStream_t stream, int* rc);
+
+// tg_reserve_workspace: workspace of at least `bytes` plus the tail scratch
+// for (current device, `stream`), allocated now; later calls on the stream
+// neither allocate nor synchronise.
+int reserve_workspace(cudaStream_t stream, size_t bytes);
+// Device allocations made by the library so far.
+uint64_t alloc_count();
 
 // Scratch for the tail split of the persistent GEMM (partial tiles of the
-// last wave's K pieces, and their flags), one set per (device, stream) so
-// that calls on different streams never share it.  Allocated on the first
-// call that splits on that stream; the flags start at zero and every launch
-// leaves them at zero.  false if it cannot be had (the call then runs
-// without a split).
+// last wave's K pieces, and their arrival counters), one set per (device,
+// stream) so that calls on different streams never share it.  Allocated by a
+// reservation or on the first call that splits on that stream; the counters
+// start at zero and every launch leaves them at zero.  false if it cannot be
+// had (the call then runs without a split).
 constexpr size_t kTailPartialBytes = size_t{20} << 20;   // >= 152 slots of 128 KiB
 constexpr int kTailFlagWords = 1024;
-bool tail_scratch(cudaStream_t stream, float** partials, uint32_t** flags);
-// Zero the tail flags of the current device (after a device-side error, a
+bool tail_scratch(cudaStream_t stream, float** partials, uint32_t** counters);
+// Zero the tail counters of the current device (after a device-side error, a
 // launch may have left some set).
 void reset_tail_flags();
+
+// True when every pointer is an allocation of the current device (false for
+// host, managed or another device's memory, and when that cannot be told).
+bool operands_local(const void* const* ptrs, int n);
+// Whether gemm_bf16 runs multicast clusters for these operands: asked for by
+// the flag, or chosen for short K without pairs -- and only over memory of the
+// current device.
+bool bf16_uses_multicast(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                         bool pair, bool mcast_flag);
 
 // Tail split (K pieces per leftover tile, 1 = none) the dense bf16 kernel
 // uses for this shape on the context's device; negative status on failure.
@@ -87,18 +104,21 @@ int launch_gemm_bf16_repitched(const Bf16Repitch& rp, const void* A, int64_t lda
                                int d_dtype, const Epi& epi, bool pair, bool mcast,
                                void* workspace, cudaStream_t stream, DeviceCtx* ctx);
 
+// no_scratch: the caller must not allocate (the static-scratch entry point),
+// so nothing that allocates (the tail split's scratch) may be turned on.
 int launch_gemm_mxfp8_impl(const void* A, int64_t lda, const void* B, int64_t ldb,
                            const void* SFA, int64_t ld_sfa, const void* SFB, int64_t ld_sfb,
                            void* D, int64_t ldd, int M, int N, int K, int d_dtype,
                            const Epi& epi, bool pair, bool mcast, uint8_t* sf_workspace,
-                           cudaStream_t stream, DeviceCtx* ctx);
+                           cudaStream_t stream, DeviceCtx* ctx, bool no_scratch = false);
 
 // Any block-scaled kind; sf_workspace holds blockscaled_workspace_bytes().
 int launch_gemm_blockscaled_impl(int kind, const void* A, int64_t lda, const void* B,
                                  int64_t ldb, const void* SFA, int64_t ld_sfa, const void* SFB,
                                  int64_t ld_sfb, void* D, int64_t ldd, int M, int N, int K,
                                  int d_dtype, const Epi& epi, bool pair, bool mcast,
-                                 uint8_t* sf_workspace, cudaStream_t stream, DeviceCtx* ctx);
+                                 uint8_t* sf_workspace, cudaStream_t stream, DeviceCtx* ctx,
+                                 bool no_scratch = false);
 
 // Host-side argument checks of a block-scaled call of `kind` (no CUDA calls).
 int check_blockscaled_args(int kind, const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -199,31 +199,18 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, co
   return false;
 }
 
-// Bounded wait until a global flag written by another CTA of the same grid
-// equals `value` (acquire at GPU scope).  The writer sets it after its data
-// (release); the caller may then read that data with L1-bypassing loads.
-static __device__ __noinline__ bool flag_wait_eq(const uint32_t* flag, uint32_t value,
-                                                 const WaitGuard g, uint32_t site) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t spin = 1; spin != 0; ++spin) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v == value) return true;
-    if ((spin & 15u) == 0) {
-      if (*g.abort_flag) return false;
-      if (global_timer_ns() - t0 > g.timeout_ns) {
-        report_timeout(g, site);
-        return false;
-      }
-    }
-    __nanosleep(64);
-  }
-  report_timeout(g, site);
-  return false;
-}
-
-__device__ __forceinline__ void flag_set_release(uint32_t* flag, uint32_t value) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(value) : "memory");
+// Arrival on a global counter shared by the CTAs of a grid: adds 1 and
+// returns the previous value, ordered after this thread's earlier memory
+// operations and before its later ones at GPU scope (acq_rel).  Nobody waits
+// on the counter: whichever arrival completes the count does the follow-up
+// work, so no CTA depends on another being resident.
+__device__ __forceinline__ uint32_t arrive_counter_gpu(uint32_t* counter) {
+  uint32_t prev;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+               : "=r"(prev)
+               : "l"(counter)
+               : "memory");
+  return prev;
 }
 
 // Bounded wait used only on the way out after a give-up: waits for copies or

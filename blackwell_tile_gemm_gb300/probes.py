@@ -29,6 +29,7 @@ def _L():
             "tg_probe_wait_timeout": [ctypes.c_uint64, vp],
             "tg_probe_mma_rate": [i32, i32, i32, vp, vp],
             "tg_probe_tmem_shapes": [vp, vp],
+            "tg_probe_hold_sms": [i32, ctypes.c_uint64, vp],
         }.items():
             f = getattr(L, name)
             f.restype = i32
@@ -93,3 +94,9 @@ def mma_rate(kind, iters, ctas, cycles, stream=None):
     """Back-to-back tcgen05.mma rate probe; cycles: int64 CUDA tensor [2*ctas] (cycles, ns)."""
     _check(_L().tg_probe_mma_rate(int(kind), int(iters), int(ctas), cycles.data_ptr(),
                                   _stream_handle(stream)), "tg_probe_mma_rate")
+
+
+def hold_sms(blocks, ns, stream=None):
+    """Occupy `blocks` SMs for `ns` nanoseconds (a test aid, see tgemm_probes.h)."""
+    _check(_L().tg_probe_hold_sms(int(blocks), int(ns), _stream_handle(stream)),
+           "tg_probe_hold_sms")

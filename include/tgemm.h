@@ -20,15 +20,26 @@
  *
  * Conventions shared by every call:
  *   - Ownership: the caller allocates and owns every buffer it passes.  The
- *     library keeps its own workspace per (device, stream) -- scale images
- *     of the block-scaled calls, gathered or re-pitched rows, the skinny
- *     call's f32 partial sums -- allocated on the first call on a stream
- *     that needs it, grown on demand (growing synchronises that stream, so
- *     make the largest call on a stream before capturing it into a graph),
- *     never shrunk, freed at process exit.  Calls on different streams never
- *     share workspace.  The transpose allocates nothing.  A CUDA graph
- *     captured from a stream keeps that stream's workspace addresses: do not
- *     replay it concurrently with itself or with other work on that stream.
+ *     library keeps its own device memory per (device, stream): a workspace
+ *     (scale images of the block-scaled calls, gathered or re-pitched rows,
+ *     the skinny call's f32 partial sums) and the tail split's scratch (see
+ *     "Tail split").  Calls on different streams never share it; it is never
+ *     shrunk and lives until process exit.  The transpose allocates nothing.
+ *   - Reserved workspace (see tg_reserve_workspace): after a reservation on a
+ *     stream, no call on that stream allocates device memory or synchronises
+ *     anything; a call that would need more workspace than was reserved
+ *     returns TG_ERR_WORKSPACE and launches nothing.
+ *   - Without a reservation (the fallback), the first call on a stream that
+ *     needs workspace allocates it, and a later call that needs more grows
+ *     it: growing synchronises that stream (cudaStreamSynchronize), frees the
+ *     old buffer and allocates a new one, so such a call may block the host.
+ *     While the stream is being captured into a CUDA graph nothing is grown:
+ *     the call returns TG_ERR_WORKSPACE (and the tail split is skipped).
+ *     A graph captured from a stream keeps that stream's workspace addresses:
+ *     do not replay it concurrently with itself or with other work on it.
+ *   - The only calls that synchronise are tg_device_status,
+ *     tg_reserve_workspace and, without a reservation, a call that grows its
+ *     stream's workspace.
  *   - Strides are in ELEMENTS and describe row-major 2-D arrays (unit inner
  *     stride).  Pointers are device pointers and must be 16-byte aligned;
  *     every row stride times the element size must be a multiple of 16 bytes.
@@ -57,8 +68,11 @@ typedef enum {
   TG_ERR_UNSUPPORTED = 3, /* valid request outside what is implemented         */
   TG_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed                 */
   TG_ERR_TIMEOUT = 5,     /* (device) a pipeline wait passed its deadline      */
-  TG_ERR_NO_SCRATCH = 6   /* problem too large for the static scratch of
+  TG_ERR_NO_SCRATCH = 6,  /* problem too large for the static scratch of
                              gemm_mxfp8_blockscaled_noalloc                    */
+  TG_ERR_WORKSPACE = 7    /* the stream's workspace is too small and may not
+                             grow now: it is reserved, or the stream is being
+                             captured into a graph                             */
 } tg_status;
 
 /* Element type of D. */
@@ -98,12 +112,16 @@ typedef struct tg_epilogue {
  * product's last wave (after W >= 0 full waves over all co-resident units)
  * fill at most half of the units, each of them is cut into S pieces along K
  * (S <= 4, S * R <= the units, pieces of >= 4 stages) that run at the same time;
- * the pieces add their f32 partial tiles through a per-(device, stream)
- * scratch of 20 MiB plus a flag block, allocated with cudaMalloc on the
- * first call that splits on a stream (make that call before capturing the
- * stream into a CUDA graph).  Results agree with the unsplit product within
- * the tolerances above; the partials are added in a fixed order, so repeated
- * calls give identical bits.
+ * every piece writes its f32 partial tile into a per-(device, stream)
+ * scratch of 20 MiB and arrives on a counter; the piece whose arrival
+ * completes the count adds the S partials in piece order and stores D.  No
+ * piece waits for another, so the call completes however many of its CTAs
+ * are resident at once (e.g. beside kernels on other streams).  The scratch
+ * is allocated by tg_reserve_workspace, or else with cudaMalloc on the first
+ * call that splits on a stream (a stream being captured runs unsplit
+ * instead).  Results agree with the unsplit product within the tolerances
+ * above; the partials are added in a fixed order, so repeated calls give
+ * identical bits.
  */
 
 /* Launch flags (bit set). */
@@ -119,7 +137,13 @@ enum {
                             gemm_bf16 with flags 0 picks these by itself for
                             K <= 1536 with M, N >= 3000, where they measured
                             6-30% faster (slower at K >= 2048).  Same
-                            results either way.                              */
+                            results either way.  Multicast clusters (asked
+                            for or chosen) run only when A and B (and the
+                            scale arrays) are allocations of the current
+                            device (cudaPointerGetAttributes); for host,
+                            managed or another GPU's memory the call runs
+                            the plain kernel instead.  This library is
+                            single-GPU code: one process drives one GPU.     */
   TG_FLAG_GATHER_TMA = 4u /* gemm_bf16_gather only: load the gathered A rows
                             inside the GEMM with TMA tile::gather4 instead
                             of copying them into the workspace first.  Same
@@ -236,8 +260,60 @@ int gemm_bf16_gather(const void* A, int64_t lda, int64_t a_rows, const int32_t* 
 
 /* tg_gemm_tail_split -- the number of K pieces (1: none) into which
  * gemm_bf16 cuts each tile for this shape on the current device (flags: 0 or
- * TG_FLAG_CTA_PAIR); minus a status code on failure.  See "Tail split". */
+ * TG_FLAG_CTA_PAIR), for operands in the current device's memory (a stream
+ * being captured without tail scratch runs unsplit); minus a status code on
+ * failure.  See "Tail split". */
 int tg_gemm_tail_split(int64_t M, int64_t N, int64_t K, unsigned flags);
+
+/* tg_gemm_multicast -- 1 if gemm_bf16 / gemm_bf16_ex with these operands,
+ * sizes and flags (0, TG_FLAG_CTA_PAIR, TG_FLAG_MULTICAST or both) run
+ * multicast clusters, 0 if they run the plain kernel (in particular when A or
+ * B is not an allocation of the current device, or that cannot be told);
+ * minus a status code for invalid arguments.  Reads pointer attributes only:
+ * nothing is launched or dereferenced. */
+int tg_gemm_multicast(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                      unsigned flags);
+
+/* Call kinds for tg_workspace_bytes. */
+enum {
+  TG_CALL_GEMM_BF16 = 0,        /* gemm_bf16, gemm_bf16_ex                     */
+  TG_CALL_GEMM_MXFP8 = 1,       /* gemm_mxfp8_blockscaled(_ex)                 */
+  TG_CALL_GEMM_MXFP4 = 2,       /* gemm_mxfp4_blockscaled                      */
+  TG_CALL_GEMM_NVFP4 = 3,       /* gemm_nvfp4_blockscaled                      */
+  TG_CALL_GEMM_BF16_SKINNY = 4, /* gemm_bf16_skinny                            */
+  TG_CALL_GEMM_BF16_GATHER = 5  /* gemm_bf16_gather (M = gathered rows)        */
+};
+
+/*
+ * tg_workspace_bytes -- bytes of stream workspace one call of kind `call`
+ * needs for these sizes: lda, ldb (elements, as passed to the call; used by
+ * the bf16 re-pitch rule), d_dtype and epi_op (used by the skinny call) and
+ * flags (TG_FLAG_CTA_PAIR; TG_FLAG_GATHER_TMA for the gather call).  Calls on
+ * one stream run in order and reuse the workspace from its start, so a
+ * stream needs the maximum over its calls, not the sum.  The tail split's
+ * scratch is separate (tg_reserve_workspace always adds it).  Minus a status
+ * code for invalid arguments.  Host arithmetic only: no CUDA call.
+ */
+int64_t tg_workspace_bytes(int call, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                           int d_dtype, int epi_op, unsigned flags);
+
+/*
+ * tg_reserve_workspace -- allocate now, for the current device and
+ * `cuda_stream`, a workspace of at least `bytes` (e.g. the maximum of
+ * tg_workspace_bytes over the calls the stream will make) and the tail
+ * split's scratch, then mark the stream reserved: from then on no call on
+ * it allocates device memory or synchronises, and one needing more workspace
+ * returns TG_ERR_WORKSPACE.  May be called again to grow the reservation.
+ * Synchronises the stream.  TG_ERR_WORKSPACE while the stream is being
+ * captured; TG_ERR_CUDA if an allocation fails; TG_ERR_INVALID_ARG for
+ * bytes < 0.
+ */
+int tg_reserve_workspace(void* cuda_stream, int64_t bytes);
+
+/* Number of device allocations (cudaMalloc) the library has made since it
+ * was loaded, over all devices and streams: workspace and tail scratch.  A
+ * caller can check that a code section allocated nothing. */
+uint64_t tg_workspace_alloc_count(void);
 
 /* tg_gemm_repitch -- which operands gemm_bf16 / gemm_bf16_ex re-pitch for
  * this shape and these row strides (see gemm_bf16): bit 0 A, bit 1 B (0:
@@ -334,7 +410,7 @@ int tile_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out,
  * outputs incomplete and released its tensor memory), or TG_ERR_CUDA when
  * the synchronisation itself failed.  `site` (may be NULL) receives the code
  * of the wait that expired.  After an error it also clears the library's
- * cross-CTA flags on this device (see "Tail split" above); other streams of
+ * tail-split counters on this device (see "Tail split" above); other streams of
  * the device should be idle at that point.
  */
 int tg_device_status(void* cuda_stream, uint32_t* site);

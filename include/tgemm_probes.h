@@ -85,6 +85,13 @@ int tg_probe_tmem_shapes(uint32_t* out, void* cuda_stream);
 int tg_probe_mma_rate(int kind, int iters, int ctas, unsigned long long* cycles,
                       void* cuda_stream);
 
+/* Occupies SMs: `blocks` (1..4096) blocks of one warp, each with 200 KB of
+ * dynamic shared memory (so that no GEMM CTA fits beside it), sleep until
+ * `ns` (1..10^9) nanoseconds have passed.  Used to show that a GEMM launched
+ * meanwhile on another stream completes while only some of its CTAs can be
+ * resident.  Not part of the contraction: a test aid. */
+int tg_probe_hold_sms(int blocks, uint64_t ns, void* cuda_stream);
+
 /* Waits on an mbarrier that nothing completes, with deadline `timeout_ns`
  * (1..10^9); the bounded wait gives up and records TG_ERR_TIMEOUT with site
  * code 99 in the status word that tg_device_status() returns. */

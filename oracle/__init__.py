@@ -447,11 +447,13 @@ def tmem_register_coord_16x32bx2(lane: int, reg: int, split_lanes: int,
     return split_lanes + row, split_cols + reg
 
 
-def block_scale_tmem_slot(row: int, sf: int = 0) -> tuple[int, int]:
+def block_scale_tmem_slot(row: int, sf: int = 0, replica: int = 0) -> tuple[int, int]:
     """(TMEM lane, byte column) holding scale ``sf`` of scale row ``row``.
 
     "tcgen05.mma", section "Weight-stationary and block scaling": scale row r
-    uses lane r % 32 and byte-column 4 * (r // 32) + sf (and is replicated in
-    the three other 32-lane slabs).
+    uses lane r % 32 and byte-column 4 * (r // 32) + sf, with four replicas
+    spaced 32 lanes apart (``replica`` 0..3 selects one).
     """
-    return row % 32, 4 * (row // 32) + sf
+    if not 0 <= replica < 4:
+        raise ValueError("four replicas, 32 lanes apart")
+    return 32 * replica + row % 32, 4 * (row // 32) + sf

@@ -77,3 +77,16 @@ def sample_indices(n: int, count: int, seed: int, tile: int) -> np.ndarray:
         edges = edges[np.linspace(0, edges.size - 1, count // 2).astype(np.int64)]
     rand = rng.choice(n, size=min(n, count - edges.size), replace=False)
     return np.unique(np.concatenate([edges, rand]).astype(np.int64))
+
+
+def edge_sample(n: int, count: int, seed: int, tile: int = 128) -> np.ndarray:
+    """Every index on either side of a tile boundary (multiples of `tile`), 0
+    and n - 1, then seeded random indices up to `count` in all."""
+    edges = {0, n - 1}
+    for t in range(tile, n, tile):
+        edges.update((t - 1, t))
+    edges = np.array(sorted(i for i in edges if 0 <= i < n), dtype=np.int64)
+    rest = np.setdiff1d(np.arange(n, dtype=np.int64), edges)
+    k = max(0, min(rest.size, count - edges.size))
+    rand = np.random.default_rng(seed).choice(rest, size=k, replace=False)
+    return np.unique(np.concatenate([edges, rand]))

@@ -14,6 +14,15 @@ than against itself.
   Compute, and Store Example": A = arange(768) as float32 (2, 32, 3, 4);
   the result is A + 1.  Stored as the flat list of expected values.
 
+Two fixtures here are written by hand, not by this script, because the
+pages state them as rules rather than as arrays:
+
+* block_scale_tmem_slots.txt -- "tcgen05.mma", section "Weight-stationary and
+  block scaling": TMEM lane and byte column of a scale row's factor, with its
+  four replicas, for selected rows.
+* ldmatrix_x2_address_providers.txt -- "ldmatrix / stmatrix", the operand
+  example's sentence on which lanes provide which row addresses.
+
 Run: python tests/golden/make_golden.py
 """
 import os

@@ -194,3 +194,56 @@ def test_repitch_rule(L, shape, lds, want):
 
 def test_repitch_rejects_negative_sizes(L):
     assert L.tg_gemm_repitch(-1, 8, 8, 8, 8) == -tg.TG_ERR_INVALID_ARG
+
+
+def test_multicast_query_falls_back_for_unknown_pointers(L):
+    # A fake address is no allocation of a current device (on a host without
+    # a GPU there is none): the short-K product and an explicit multicast
+    # request both answer "plain kernel".
+    assert L.tg_gemm_multicast(A16, A16, 4000, 3000, 1000, 0) == 0
+    assert L.tg_gemm_multicast(A16, A16, 4000, 3000, 1000, tg.TG_FLAG_MULTICAST) == 0
+    assert L.tg_gemm_multicast(A16, A16, 8192, 8192, 8192,
+                               tg.TG_FLAG_MULTICAST | tg.TG_FLAG_CTA_PAIR) == 0
+    # shapes that never ask for multicast, and empty ones
+    assert L.tg_gemm_multicast(A16, A16, 4000, 3000, 4096, 0) == 0
+    assert L.tg_gemm_multicast(A16, A16, 4000, 3000, 0, tg.TG_FLAG_MULTICAST) == 0
+    assert L.tg_gemm_multicast(A16, A16, -1, 3000, 1000, 0) == -tg.TG_ERR_INVALID_ARG
+    assert L.tg_gemm_multicast(A16, A16, 64, 64, 64, 8) == -tg.TG_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("call,shape,lds,d,epi,flags,want", [
+    # re-pitched 16-byte rows: (M + N) rows of ceil(K/64)*64 bf16 elements
+    (tg.TG_CALL_GEMM_BF16, (4000, 3000, 1000), (1000, 1000), 0, 0, 0, (4000 + 3000) * 1024 * 2),
+    (tg.TG_CALL_GEMM_BF16, (4000, 3000, 1000), (1024, 1024), 0, 0, 0, 0),
+    # scale images: (ceil(M/r)*r/128 + 2*ceil(N/256)) * ceil(K/stage) * V * 512
+    (tg.TG_CALL_GEMM_MXFP8, (8192, 8192, 8192), (8192, 8192), 1, 0, 1, 4 << 20),
+    (tg.TG_CALL_GEMM_MXFP8, (300, 264, 160), (160, 160), 0, 0, 0, (3 + 4) * 2 * 512),
+    (tg.TG_CALL_GEMM_MXFP4, (8192, 8192, 8192), (4096, 4096), 1, 0, 1, 4 << 20),
+    (tg.TG_CALL_GEMM_NVFP4, (8192, 8192, 8192), (4096, 4096), 1, 0, 1, 8 << 20),
+    # skinny: f32 partial sums only for bf16 D (M * ceil(N/4)*4 * 4 bytes)
+    (tg.TG_CALL_GEMM_BF16_SKINNY, (16, 8192, 8192), (8192, 8192), 1, 0, 0, 16 * 8192 * 4),
+    (tg.TG_CALL_GEMM_BF16_SKINNY, (16, 8192, 8192), (8192, 8192), 0, 0, 0, 0),
+    # gathered rows at a 128-byte pitch, unless gather4 loads them in the GEMM
+    (tg.TG_CALL_GEMM_BF16_GATHER, (4096, 8192, 8192), (8192, 8192), 1, 0, 0, 4096 * 8192 * 2),
+    (tg.TG_CALL_GEMM_BF16_GATHER, (4096, 8192, 8192), (8192, 8192), 1, 0,
+     tg.TG_FLAG_GATHER_TMA, 0),
+])
+def test_workspace_bytes(L, call, shape, lds, d, epi, flags, want):
+    assert tg.workspace_bytes(call, *shape, *lds, d, epi, flags) == want
+
+
+def test_workspace_bytes_rejects_bad_requests(L):
+    f = L.tg_workspace_bytes
+    assert f(99, 64, 64, 64, 64, 64, 0, 0, 0) == -tg.TG_ERR_INVALID_ARG
+    assert f(tg.TG_CALL_GEMM_MXFP8, 64, 64, 48, 64, 64, 0, 0, 0) == -tg.TG_ERR_INVALID_ARG
+    assert f(tg.TG_CALL_GEMM_BF16_SKINNY, 129, 64, 64, 64, 64, 0, 0, 0) == -tg.TG_ERR_UNSUPPORTED
+    assert f(tg.TG_CALL_GEMM_BF16, -1, 64, 64, 64, 64, 0, 0, 0) == -tg.TG_ERR_INVALID_ARG
+    assert f(tg.TG_CALL_GEMM_BF16, 0, 64, 64, 64, 64, 0, 0, 0) == 0
+
+
+def test_reserve_workspace_host_checks(L):
+    assert L.tg_reserve_workspace(None, -1) == tg.TG_ERR_INVALID_ARG
+    assert "workspace" in tg.status_string(tg.TG_ERR_WORKSPACE)
+    before = L.tg_workspace_alloc_count()
+    # the host checks above allocate nothing
+    assert L.tg_workspace_alloc_count() == before

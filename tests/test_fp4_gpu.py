@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 from blackwell_tile_gemm_gb300 import synth
-from tests._gpu import assert_within, dev_u8, host_values, sample_indices, torch_cuda
+from tests._gpu import assert_within, dev_u8, edge_sample, host_values, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -138,8 +138,8 @@ def test_fp4_8k_workload_sampled(tg, oracle, kind):
     w = synth.WORKLOADS[KINDS[kind][2]]
     x = synth.make_inputs(w)
     got = host_values(run_fp4(tg, kind, x["A"], x["B"], x["SFA"], x["SFB"], "bf16", True))
-    rows = sample_indices(w.M, 96, 15, 256)
-    cols = sample_indices(w.N, 96, 16, 256)
+    rows = edge_sample(w.M, 256, 15)
+    cols = edge_sample(w.N, 256, 16)
     ref, mag = oracle_fp4(oracle, kind, x, rows=rows)
     assert_within(got[rows], ref, mag, True, f"{kind} 8k rows")
     ref, mag = oracle_fp4(oracle, kind, x, cols=cols)

@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 
 from blackwell_tile_gemm_gb300 import synth
-from tests._gpu import assert_within, dev_bf16, dev_u8, host_values, sample_indices, torch_cuda
+from tests._gpu import (assert_within, dev_bf16, dev_u8, edge_sample, host_values, sample_indices,
+                        torch_cuda)
 
 pytestmark = pytest.mark.gpu
 
@@ -222,27 +223,33 @@ def test_block_scaled_calls_on_two_streams(tg, oracle):
         assert_within(host_values(D), ref, mag, False, "two streams")
 
 
-def _sampled(tg, oracle, name, out, pair, tile_m):
-    w = synth.WORKLOADS[name]
-    x = synth.make_inputs(name)
-    D = run_bf16(tg, x["A"], x["B"], out, pair=pair)
-    got = host_values(D)
-    rows = sample_indices(w.M, 96, 11, tile_m)
-    cols = sample_indices(w.N, 96, 12, 256)
-    ref, mag = oracle.gemm_bf16(x["A"], x["B"], rows=rows)
-    assert_within(got[rows], ref, mag, out == "bf16", f"{name} rows")
-    ref, mag = oracle.gemm_bf16(x["A"], x["B"], cols=cols)
-    assert_within(got[:, cols], ref, mag, out == "bf16", f"{name} cols")
-
-
 @pytest.mark.slow
-def test_sq4k_workload_sampled(tg, oracle):
-    _sampled(tg, oracle, "sq4k", "bf16", False, 128)
+def test_sq4k_workload_every_element(tg, oracle):
+    # 4096^3, bf16 D, single-CTA 128 x 256 tiles (the workload's own kernel):
+    # every element of D against the float64 oracle.
+    w = synth.WORKLOADS["sq4k"]
+    assert not w.cta_pair
+    x = synth.make_inputs("sq4k")
+    got = host_values(run_bf16(tg, x["A"], x["B"], "bf16", pair=False))
+    ref, mag = oracle.gemm_bf16(x["A"], x["B"])
+    assert_within(got, ref, mag, True, "sq4k every element")
 
 
 @pytest.mark.slow
 def test_sq8k_workload_sampled(tg, oracle):
-    _sampled(tg, oracle, "sq8k", "f32", True, 256)
+    # 8192^3 in CTA pairs, f32 D: 256 full rows and 256 full columns of D,
+    # including every row and column on either side of each 128 boundary
+    # (CTA rows of a pair, B halves, tile edges).
+    w = synth.WORKLOADS["sq8k"]
+    x = synth.make_inputs("sq8k")
+    got = host_values(run_bf16(tg, x["A"], x["B"], "f32", pair=True))
+    rows = edge_sample(w.M, 256, 11)
+    cols = edge_sample(w.N, 256, 12)
+    assert rows.size == 256 and cols.size == 256
+    ref, mag = oracle.gemm_bf16(x["A"], x["B"], rows=rows)
+    assert_within(got[rows], ref, mag, False, "sq8k rows")
+    ref, mag = oracle.gemm_bf16(x["A"], x["B"], cols=cols)
+    assert_within(got[:, cols], ref, mag, False, "sq8k cols")
 
 
 # ------------------------------------------------------------------ MXFP8
@@ -301,8 +308,8 @@ def test_mx8k_workload_sampled(tg, oracle):
     w = synth.WORKLOADS["mx8k"]
     x = synth.make_inputs("mx8k")
     got = host_values(run_mx(tg, x["A"], x["B"], x["SFA"], x["SFB"], "bf16", pair=True))
-    rows = sample_indices(w.M, 96, 13, 256)
-    cols = sample_indices(w.N, 96, 14, 256)
+    rows = edge_sample(w.M, 256, 13)
+    cols = edge_sample(w.N, 256, 14)
     ref, mag = oracle.gemm_mxfp8(x["A"], x["B"], x["SFA"], x["SFB"], rows=rows)
     assert_within(got[rows], ref, mag, True, "mx8k rows")
     ref, mag = oracle.gemm_mxfp8(x["A"], x["B"], x["SFA"], x["SFB"], cols=cols)

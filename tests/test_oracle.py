@@ -511,6 +511,39 @@ def test_block_scale_slots_cover_128_rows(oracle):
     assert {s[1] for s in slots} == {0, 4, 8, 12}
 
 
+def test_block_scale_slots_match_the_page_rows(oracle):
+    # Rows of the "tcgen05.mma" block-scaling rule written out by hand in the
+    # fixture: lane r % 32 plus the four 32-lane replicas, byte column
+    # 4 * (r // 32) + sf.  A transposed map (lane (r // 4) % 32, byte 4 * (r % 4))
+    # or a missing replica fails here.
+    rows = np.loadtxt(os.path.join(GOLDEN, "block_scale_tmem_slots.txt"), dtype=np.int64)
+    assert rows.shape[1] == 7 and len(rows) >= 16
+    for r, sf, l0, l1, l2, l3, col in rows:
+        got = [oracle.block_scale_tmem_slot(int(r), int(sf), q) for q in range(4)]
+        assert got == [(int(l0), int(col)), (int(l1), int(col)), (int(l2), int(col)),
+                       (int(l3), int(col))], (r, sf)
+    with pytest.raises(ValueError):
+        oracle.block_scale_tmem_slot(0, 0, 4)
+
+
+def test_ldmatrix_address_providers_match_the_page_example(oracle):
+    # The x2 operand-specification example: with S_std[k, m, r, w] =
+    # SM[2r + m, w, k], lanes 0..15 supply the fixture's original rows and
+    # lanes 16..31 repeat addresses that lanes 0..15 supply.
+    table = np.loadtxt(os.path.join(GOLDEN, "ldmatrix_x2_address_providers.txt"),
+                       dtype=np.int64)
+    assert table.shape == (16, 4)
+    def sm_row(lane):
+        m, r = oracle.ldmatrix_address_row(lane, 2)
+        return 2 * r + m
+    for lane, m, r, orig in table:
+        assert oracle.ldmatrix_address_row(int(lane), 2) == (int(m), int(r))
+        assert sm_row(int(lane)) == int(orig)
+    valid = {int(o) for o in table[:, 3]}
+    assert valid == set(range(16))
+    assert all(sm_row(lane) in valid for lane in range(16, 32))
+
+
 def test_add_one_worked_example(oracle):
     a = np.arange(768, dtype=np.float32).reshape(2, 32, 3, 4)
     golden = np.loadtxt(os.path.join(GOLDEN, "add_one_2x32x3x4.txt"), dtype=np.float32)
