@@ -487,13 +487,15 @@ def run_ours(args):
 
     # Check the timed work: the last step's outputs against the oracle on the
     # CPU-baseline sample (and the transpose against a host transpose).
+    # (The end-to-end loop runs first: the oracle's host threads and buffers
+    # would otherwise share the host's memory system with its copies.)
+    e2e = measure_e2e(torch, tg, host, dev, stream, args.e2e_steps if args.kernel == "all" else 0,
+                      flops_step)
     parity = None
     cpu = None
     if args.kernel == "all":
         cpu, samples = cpu_baseline(args.cpu_seconds)
         parity = step_parity(torch, d, host, samples)
-    e2e = measure_e2e(torch, tg, host, dev, stream, args.e2e_steps if args.kernel == "all" else 0,
-                      flops_step)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT if flops_step else "GB/s", "n_gpus": 1,
