@@ -316,19 +316,27 @@ def make_step_inputs(torch, dev):
 
 
 def probe_rates(torch, dev):
-    """Dense FLOP per SM per clock of the tensor pipe, measured live by the
-    library's rate probe (back-to-back MMAs on every SM, no memory traffic):
-    bf16 kind::f16 and E4M3 block-scaled kind::mxf8f6f4."""
+    """The tensor pipe's own rate, measured live by the library's rate probe
+    (back-to-back MMAs on every SM, no memory traffic) for bf16 kind::f16 and
+    E4M3 block-scaled kind::mxf8f6f4: dense FLOP per SM per clock, the SM
+    clock the probe itself ran at (its cycle counter over its elapsed
+    nanoseconds) and the resulting chip rate.  Run right after the timed
+    region, at a similar length (~0.6 ms), so that it sees the same power
+    state; the SM cycle counter, not NVML's clock reading, gives the clock
+    under tensor load."""
     from blackwell_tile_gemm_gb300 import probes
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out = {}
-    for name, kind, k in (("bf16", 0, 16), ("mxfp8", 1, 32)):
-        iters = 2048
+    for name, kind, k, iters in (("bf16", 0, 16, 2048), ("mxfp8", 1, 32, 1024)):
         cyc = torch.zeros(2 * sms, dtype=torch.int64, device=dev)
         probes.mma_rate(kind, iters, sms, cyc)
         torch.cuda.synchronize()
-        c = cyc.view(sms, 2)[:, 0].double().median().item()
-        out[name] = 2 * 128 * 256 * k * 4 * iters / c
+        v = cyc.view(sms, 2).double()
+        c = v[:, 0].median().item()
+        ns = v[:, 1].median().item()
+        rate = 2 * 128 * 256 * k * 4 * iters / c
+        out[name] = {"flop_per_clk_per_sm": rate, "mhz": 1e3 * c / ns,
+                     "tflops": sms * rate * (c / ns) * 1e9 / 1e12}
     return sms, out
 
 
@@ -379,7 +387,6 @@ def run_ours(args):
         if ev is not None:
             ev[3].record(stream)
 
-    sms, rates = probe_rates(torch, dev)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -400,6 +407,7 @@ def run_ours(args):
         t_end.record(stream)
         torch.cuda.synchronize()
         time.sleep(0.002)
+    sms, probe = probe_rates(torch, dev)
     total_ms = t_start.elapsed_time(t_end)
     code, site = tg.tg_device_status()
     if code != tg.TG_OK:
@@ -424,10 +432,8 @@ def run_ours(args):
         n: [(float(starts[k, i]), float(starts[k, i + 1])) for k in range(args.steps)]
         for i, n in enumerate(names)})
 
-    def theoretical(tflops, rate, mhz):
-        if not mhz:
-            return None
-        return tflops * 1e12 / (sms * rate * mhz * 1e6)
+    def theoretical(tflops, kind):
+        return tflops / probe[kind]["tflops"]
 
     kern = {}
     if run_bf16:
@@ -435,14 +441,14 @@ def run_ours(args):
         c = clk_by_kernel["gemm_bf16"]
         kern["gemm_bf16"] = {"ms": bf16_ms, "tflops": t, "frac_of_bf16_peak": t / peak_bf16,
                              "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"],
-                             "frac_theoretical": theoretical(t, rates["bf16"], c["sm_mhz"])}
+                             "frac_theoretical": theoretical(t, "bf16")}
     if run_mx:
         t = flops_gemm / (mx_ms * 1e-3) / 1e12
         c = clk_by_kernel["gemm_mxfp8_blockscaled"]
         kern["gemm_mxfp8_blockscaled"] = {
             "ms": mx_ms, "tflops": t, "frac_of_2x_bf16_peak": t / (2 * peak_bf16),
             "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"],
-            "frac_theoretical": theoretical(t, rates["mxfp8"], c["sm_mhz"])}
+            "frac_theoretical": theoretical(t, "mxfp8")}
     if run_f4:
         t = flops_gemm / (mx_ms * 1e-3) / 1e12
         c = clk_by_kernel[names[1]]
@@ -474,16 +480,20 @@ def run_ours(args):
                 "traffic": profiled_traffic(dominant) if SIZE == 8192 else None,
                 "peak_source": peak_note}
     if dominant in ("gemm_bf16", "gemm_mxfp8_blockscaled"):
-        rate = rates["bf16" if dominant == "gemm_bf16" else "mxfp8"]
-        mhz = kern[dominant]["sm_mhz"]
+        kind = "bf16" if dominant == "gemm_bf16" else "mxfp8"
+        pr = probe[kind]
         max_mhz = clk.summary()["sm_max_mhz"] or 2070.0
+        at_max = sms * pr["flop_per_clk_per_sm"] * max_mhz * 1e6 / 1e12
         roofline.update({
-            "frac_theoretical": theoretical(achieved, rate, mhz),
-            "theoretical_peak": sms * rate * mhz * 1e6 / 1e12 if mhz else None,
-            "frac_theoretical_at_max_clock": theoretical(achieved, rate, max_mhz),
-            "theoretical_basis": (f"{sms} SMs x {rate:.0f} FLOP/clk/SM (rate probe, "
-                                  f"back-to-back tcgen05.mma) x the median SM clock sampled "
-                                  f"while the kernel ran ({mhz} MHz)")})
+            "frac_theoretical": achieved / pr["tflops"],
+            "theoretical_peak": pr["tflops"],
+            "frac_theoretical_at_max_clock": achieved / at_max,
+            "theoretical_basis": (
+                f"{sms} SMs x {pr['flop_per_clk_per_sm']:.0f} FLOP/clk/SM x {pr['mhz']:.0f} MHz: "
+                f"the rate probe's back-to-back tcgen05.mma on every SM, at the SM clock its "
+                f"cycle counter showed (NVML reports {max_mhz:.0f} MHz meanwhile; the SM cycle "
+                f"counter runs slower under tensor load); at {max_mhz:.0f} MHz the peak would "
+                f"be {at_max:.0f} TFLOP/s")})
 
     # Check the timed work: the last step's outputs against the oracle on the
     # CPU-baseline sample (and the transpose against a host transpose).
@@ -513,7 +523,7 @@ def run_ours(args):
         "gpu_launches": (int(run_bf16) + 2 * int(run_mx) + 2 * int(run_f4) + int(run_tr))
         * args.steps,
         "clocks": clk.summary(),
-        "tensor_pipe_probe": {"sms": sms, "flop_per_clk_per_sm": rates},
+        "tensor_pipe_probe": {"sms": sms, **probe},
     }
     if parity is not None:
         line["parity"] = parity

@@ -13,8 +13,6 @@
 namespace tg {
 
 namespace {
-// m-tiles per band of the persistent tile order.
-constexpr int kRasterGroup = 8;
 using CfgF32 = GemmCfg<1, kKindBf16, 256, 2, 4, false>;
 using CfgBf16 = GemmCfg<1, kKindBf16, 256, 2, 4, true>;
 using CfgPairF32 = GemmCfg<2, kKindBf16, 256, 2, 6, false>;
@@ -68,7 +66,6 @@ int launch_gemm_bf16_impl(const void* A, int64_t lda, const void* B, int64_t ldb
   a.D = D;
   a.ldd = ldd;
   a.epi = epi;
-  a.raster_group = kRasterGroup;
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
   const bool bf16_out = d_dtype == TG_D_BF16;

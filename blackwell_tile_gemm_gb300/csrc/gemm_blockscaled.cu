@@ -29,8 +29,6 @@
 namespace tg {
 
 namespace {
-// m-tiles per band of the persistent tile order.
-constexpr int kRasterGroup = 8;
 
 using CfgMxF32 = GemmCfg<1, kKindMxf8, 256, 1, 4, false>;
 using CfgMxBf16 = GemmCfg<1, kKindMxf8, 256, 1, 4, true>;
@@ -199,7 +197,6 @@ int launch_gemm_blockscaled_impl(int kind, const void* A, int64_t lda, const voi
   a.epi = epi;
   a.sfa_blocks = pl.sfa_blocks;
   a.sfb_blocks = pl.sfb_blocks;
-  a.raster_group = kRasterGroup;
   a.status = ctx->status;
   a.timeout_ns = wait_timeout_ns();
   a.no_scratch = no_scratch;

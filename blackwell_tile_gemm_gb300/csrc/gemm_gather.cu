@@ -23,7 +23,6 @@
 namespace tg {
 
 namespace {
-constexpr int kRasterGroup = 8;
 using CfgGatherF32 = GemmCfg<1, kKindBf16, 256, 2, 4, false, false, true>;
 using CfgGatherBf16 = GemmCfg<1, kKindBf16, 256, 2, 4, true, false, true>;
 using CfgGatherPairF32 = GemmCfg<2, kKindBf16, 256, 2, 6, false, false, true>;
@@ -104,7 +103,6 @@ int launch_gemm_bf16_gather_impl(const void* A, int64_t lda, int a_rows, const i
   a.D = D;
   a.ldd = ldd;
   a.epi = epi;
-  a.raster_group = kRasterGroup;
   a.gather_idx = row_idx;
   a.gather_rows = a_rows;
   a.status = ctx->status;

@@ -69,6 +69,14 @@ struct GemmArgs {
   int sfa_blocks;   // 128-row blocks per K group in the SFA image
   int sfb_blocks;   // 128-row blocks per K group in the SFB image
   int raster_group; // m-tiles per band of the tile order
+  // Tile order refinements (see tile_coords and next_work): n_snake walks the
+  // n-tiles of every other band backwards, so that consecutive bands start on
+  // the B panels the previous one ended on; k_snake walks K backwards in every
+  // other wave of whole tiles, so that a unit's next tile starts on the K
+  // slices the units around it read last (a plain LRU-like cache holds those,
+  // and evicts the first slices just before the next wave would reuse them).
+  int n_snake;
+  int k_snake;
   const int* gather_idx;  // gathered A: D row i uses A row gather_idx[i] (else null)
   int gather_rows;        // rows of A; indices outside [0, gather_rows) read zeros
   // Tail split (see next_work): tiles below full_tiles are whole work items;
@@ -202,8 +210,9 @@ struct GemmCfg {
 // One work item of a unit: a whole tile, or one K piece of a tail tile.
 struct Work {
   int t;        // tile id (tile order)
-  int k0, k1;   // K stages k0, k0 + ks, ... below k1
-  int ks;
+  int k0;       // first K stage
+  int ks;       // step between K stages (negative: backwards)
+  int nk;       // number of K stages: k0, k0 + ks, ..., k0 + (nk - 1) * ks
   int piece;    // K piece (its partial's slot; the order in which partials add up)
   int tail;     // tail tile index, or -1 for a whole tile
 };
@@ -220,9 +229,10 @@ __device__ __forceinline__ bool next_work(const GemmArgs& p, int unit, int num_u
   const int t = unit + i * num_units;
   if (t < p.full_tiles) {
     w.t = t;
-    w.k0 = 0;
-    w.k1 = p.num_k_blocks;
-    w.ks = 1;
+    const bool back = p.k_snake && (i & 1);
+    w.k0 = back ? p.num_k_blocks - 1 : 0;
+    w.ks = back ? -1 : 1;
+    w.nk = p.num_k_blocks;
     w.piece = 0;
     w.tail = -1;
     return true;
@@ -237,16 +247,16 @@ __device__ __forceinline__ bool next_work(const GemmArgs& p, int unit, int num_u
   w.piece = unit % S;
   w.t = p.full_tiles + w.tail;
   w.k0 = w.piece;
-  w.k1 = p.num_k_blocks;
   w.ks = S;
+  w.nk = (p.num_k_blocks - w.piece + S - 1) / S;
   return true;
 }
 
 // Grouped tile order: consecutive tile ids walk down a band of `group`
 // m-tiles before moving to the next n-tile, so the CTAs that run at the same
 // time share a few A and B panels in L2.
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group, int& tm,
-                                            int& tn) {
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group, int n_snake,
+                                            int& tm, int& tn) {
   const int per_group = group * num_n;
   const int g = t / per_group;
   const int first_m = g * group;
@@ -254,6 +264,7 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   const int r = t - g * per_group;
   tm = first_m + r % gm;
   tn = r / gm;
+  if (n_snake && (g & 1)) tn = num_n - 1 - tn;
 }
 
 // Copies one stage's scale images from shared memory into its TMEM scale
@@ -560,7 +571,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int it = 0; ok && next_work(p, unit, num_units, it, w); ++it) {
         const int t = w.t;
         int tmc, tn;
-        tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
+        tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, p.n_snake, tmc, tn);
         const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
         const int a_row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM;
         const int b_row = tn * C::BN + static_cast<int>(pair_rank) * C::B_ROWS;
@@ -573,7 +584,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if (src < 0 || src >= p.gather_rows) src = p.gather_rows;
           r[j] = src;
         }
-        for (int kb = w.k0; kb < w.k1; kb += w.ks) {
+        for (int j = 0, kb = w.k0; j < w.nk; ++j, kb += w.ks) {
           int got = 1;
           if (lane == 0)
             got = (mbar_try_wait(empty0 + 8u * stage, phase ^ 1u) ||
@@ -645,13 +656,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int it = 0; ok && next_work(p, unit, num_units, it, w); ++it) {
         const int t = w.t;
         int tmc, tn;
-        tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
+        tile_coords(t, num_mc, p.num_n_tiles, p.raster_group, p.n_snake, tmc, tn);
         const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
         const int a_row = tm * C::MMA_M + static_cast<int>(pair_rank) * C::BM;
         const int b_row = tn * C::BN + static_cast<int>(pair_rank) * C::B_ROWS;
         const int sfa_row = C::kCtaGroup == 2 ? tm * 2 + static_cast<int>(pair_rank) : tm;
         const int sfb_row = tn * (C::BN / 128);
-        for (int kb = w.k0; kb < w.k1; kb += w.ks) {
+        for (int j = 0, kb = w.k0; j < w.nk; ++j, kb += w.ks) {
           if (!mbar_try_wait(empty0 + 8u * stage, phase ^ 1u) &&
               !mbar_wait(&empty_bar[stage], phase ^ 1u, guard, kSiteProducerEmpty)) {
             ok = false;
@@ -744,7 +755,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
-        for (int kb = w.k0; kb < w.k1; kb += w.ks) {
+        for (int j = 0, kb = w.k0; j < w.nk; ++j, kb += w.ks) {
           if (!ready && !mbar_try_wait(ready0 + 8u * stage, phase) &&
               !mbar_wait(&ready_bar[stage], phase, guard, kSiteMmaFull)) {
             ok = false;
@@ -766,14 +777,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               mma_block_scaled<C::kCtaGroup, C::kKind>(
                   d_tmem, ad + 2 * k, bd + 2 * k,
                   idesc_block_scaled<C::kKind>(C::MMA_M, C::BN, sf, sf), sfa_t + 4 * g,
-                  sfb_t + 4 * g * C::kSfBlocksB, (kb != w.k0 || k != 0));
+                  sfb_t + 4 * g * C::kSfBlocksB, (j != 0 || k != 0));
               if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           } else {
 #pragma unroll
             for (int k = 0; k < C::kIssues; ++k) {
               mma_bf16<C::kCtaGroup>(d_tmem, ad + 2 * k, bd + 2 * k,
-                                     idesc_bf16_f32(C::MMA_M, C::BN), (kb != w.k0 || k != 0));
+                                     idesc_bf16_f32(C::MMA_M, C::BN), (j != 0 || k != 0));
               if (k == 0) ready = mbar_try_wait(ready0 + 8u * ns, nph);
             }
           }
@@ -822,7 +833,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         bool copied = false;
         Work w;
         for (int it = 0; ok && next_work(p, unit, num_units, it, w); ++it) {
-          for (int kb = w.k0; kb < w.k1; kb += w.ks) {
+          for (int j = 0, kb = w.k0; j < w.nk; ++j, kb += w.ks) {
             if (!mbar_try_wait(full0 + 8u * stage, phase) &&
                 !mbar_wait(&full_bar[stage], phase, guard, kSiteScaleFull)) {
               ok = false;
@@ -873,7 +884,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     Work w;
     for (int it = 0; next_work(p, unit, num_units, it, w); ++it) {
       int tmc, tn;
-      tile_coords(w.t, num_mc, p.num_n_tiles, p.raster_group, tmc, tn);
+      tile_coords(w.t, num_mc, p.num_n_tiles, p.raster_group, p.n_snake, tmc, tn);
       const int tm = tmc * C::kPairs + static_cast<int>(pair_id);
       // One lane waits for the accumulator; the others wait at the warp barrier.
       int got = 1;

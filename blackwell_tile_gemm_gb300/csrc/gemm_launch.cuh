@@ -86,6 +86,15 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
   const int num_tiles = (args.num_m_tiles + C::kPairs - 1) / C::kPairs * args.num_n_tiles;
   int units = num_tiles < units_max ? num_tiles : units_max;
   GemmArgs a = args;
+  // Tile order (measured on GB300, 8192^3 in pairs: bf16 0.583 -> 0.574 ms,
+  // DRAM reads 1096 -> 885 MB a launch; MXFP8 0.333 -> 0.326 ms; 4096^3
+  // single CTAs 0.094 -> 0.090 ms): bands of 4096 rows for CTA pairs and of
+  // 384 rows for single CTAs, n walked backwards in every other band, K
+  // backwards in every other wave.
+  a.raster_group = (C::kCtaGroup == 2 ? 4096 : 384) / (128 * C::kCtaGroup * C::kPairs);
+  if (a.raster_group < 1) a.raster_group = 1;
+  a.n_snake = 1;
+  a.k_snake = 1;
   a.full_tiles = num_tiles;
   a.tail_split = 1;
   a.tail_items = 0;

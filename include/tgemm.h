@@ -124,6 +124,17 @@ typedef struct tg_epilogue {
  * identical bits.
  */
 
+/*
+ * Result bits.  Each output tile accumulates its K range in an order fixed
+ * by the persistent schedule: forwards, or backwards in every other wave of
+ * tiles (which keeps the K slices a unit needs next in L2), and split into
+ * pieces in a tail split.  The same call (shape, flags, strides, device)
+ * therefore always returns the same bits; calls with other flags, or on a
+ * device with another SM count, may differ in the last bits, within the
+ * tolerances.  Exact inputs (every partial sum representable) give the exact
+ * result whatever the order.
+ */
+
 /* Launch flags (bit set). */
 enum {
   TG_FLAG_CTA_PAIR = 1u, /* cta_group::2: two CTAs of a cluster share one
@@ -136,8 +147,9 @@ enum {
                             only): two single CTAs, each loading half of B;
                             gemm_bf16 with flags 0 picks these by itself for
                             K <= 1536 with M, N >= 3000, where they measured
-                            6-30% faster (slower at K >= 2048).  Same
-                            results either way.  Multicast clusters (asked
+                            6-30% faster (slower at K >= 2048).  Results
+                            agree within the tolerances either way (see
+                            "Result bits" below).  Multicast clusters (asked
                             for or chosen) run only when A and B (and the
                             scale arrays) are allocations of the current
                             device (cudaPointerGetAttributes); for host,
@@ -146,8 +158,9 @@ enum {
                             single-GPU code: one process drives one GPU.     */
   TG_FLAG_GATHER_TMA = 4u /* gemm_bf16_gather only: load the gathered A rows
                             inside the GEMM with TMA tile::gather4 instead
-                            of copying them into the workspace first.  Same
-                            results; slower on large shapes (see there).   */
+                            of copying them into the workspace first.
+                            Results agree within the tolerances; slower on
+                            large shapes (see there).                       */
 };
 
 /*
