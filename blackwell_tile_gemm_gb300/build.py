@@ -1,7 +1,11 @@
 """Builds libtgemm.so in-tree for sm_103a with nvcc (no cmake, no torch extension).
 
 Each translation unit compiles in its own nvcc process, in parallel; the
-objects are linked into ``blackwell_tile_gemm_gb300/_build/libtgemm.so``.
+objects are linked into ``blackwell_tile_gemm_gb300/_build/libtgemm.so``.  The
+probe kernels (the pages' worked examples, the tensor-pipe rate probe and the
+SM occupier the tests and the benchmark use) go into a separate
+``libtgemm_probes.so`` that links against it, so the product library carries
+only the contraction's entry points.
 
     python -m blackwell_tile_gemm_gb300.build [--force] [--verbose]
 """
@@ -19,8 +23,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtgemm.so")
+PROBE_LIB = os.path.join(BUILD, "libtgemm_probes.so")
 SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_blockscaled.cu", "gemm_fp4.cu", "gemm_skinny.cu",
-           "gemm_gather.cu", "gemm_mxfp8_noalloc.cu", "transpose.cu", "probes.cu"]
+           "gemm_gather.cu", "gemm_mxfp8_noalloc.cu", "transpose.cu"]
+PROBE_SOURCES = ["probes.cu"]
 HEADERS = ["tg_ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh", "tg_internal.h", "epilogue.cuh",
            "gemm_kinds.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,14 +40,15 @@ def nvcc() -> str:
 
 
 def _inputs_mtime() -> float:
-    paths = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
+    paths = [os.path.join(CSRC, f) for f in SOURCES + PROBE_SOURCES + HEADERS]
     paths += [os.path.join(ROOT, "include", f) for f in ("tgemm.h", "tgemm_probes.h")]
     paths.append(os.path.abspath(__file__))
     return max(os.path.getmtime(p) for p in paths)
 
 
 def up_to_date() -> bool:
-    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _inputs_mtime()
+    t = _inputs_mtime()
+    return all(os.path.exists(p) and os.path.getmtime(p) >= t for p in (LIB, PROBE_LIB))
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
@@ -66,17 +73,25 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             sys.stderr.write(r.stderr)
         return obj
 
-    workers = min(len(SOURCES), max(1, os.cpu_count() or 1))
+    all_sources = SOURCES + PROBE_SOURCES
+    workers = min(len(all_sources), max(1, os.cpu_count() or 1))
     with cf.ThreadPoolExecutor(max_workers=workers) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
-    if verbose:
-        print(" ".join(cmd), flush=True)
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+        objs = dict(zip(all_sources, ex.map(compile_one, all_sources)))
+
+    def link(out, srcs, extra):
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [objs[s] for s in srcs] + extra
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link of {os.path.basename(out)} failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
+
+    link(LIB, SOURCES, [])
+    # The probes call the library's internal helpers (device context, tensor
+    # maps, the status record): link against it, found next to this file.
+    link(PROBE_LIB, PROBE_SOURCES, ["-L", BUILD, "-ltgemm", "-Xlinker", "-rpath,$ORIGIN"])
     return LIB
 
 

@@ -1,20 +1,34 @@
-"""Python binding of the probe kernels declared in include/tgemm_probes.h.
+"""Python binding of the probe kernels declared in include/tgemm_probes.h
+(``_build/libtgemm_probes.so``, which links against libtgemm.so).
 
 Each probe runs one of the pages' worked examples, or dumps one hardware
-mapping, in a single CTA; the tests compare the results with the oracle.
+mapping, in a single CTA; the tests compare the results with the oracle.  The
+rate probe and the SM occupier are measurement and test aids.
 """
 from __future__ import annotations
 
 import ctypes
+import os
+import threading
 
-from . import _check, _stream_handle, lib
+from . import _PKG, _check, _stream_handle, lib
 
+PROBE_LIB_PATH = os.path.join(_PKG, "_build", "libtgemm_probes.so")
 _ready = False
+_plib = None
+_plock = threading.Lock()
 
 
 def _L():
-    global _ready
-    L = lib()
+    global _ready, _plib
+    lib()                       # the library the probes link against, loaded first
+    with _plock:
+        if _plib is None:
+            if not os.path.exists(PROBE_LIB_PATH):
+                raise RuntimeError(f"{PROBE_LIB_PATH} is missing: build with "
+                                   "`python -m blackwell_tile_gemm_gb300.build`")
+            _plib = ctypes.CDLL(PROBE_LIB_PATH)
+    L = _plib
     if not _ready:
         vp, i32 = ctypes.c_void_p, ctypes.c_int
         for name, args in {

@@ -19,9 +19,9 @@ def L():
     return tg.lib()
 
 
-def declared_functions():
+def declared_functions(headers=HEADERS):
     names = []
-    for h in HEADERS:
+    for h in headers:
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
@@ -35,8 +35,16 @@ def test_headers_declare_the_three_entry_points():
 
 
 def test_library_exports_every_declared_symbol(L):
-    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    # tgemm.h: the product library; tgemm_probes.h: the probe library, which
+    # links against it and loads without a GPU too.
+    missing = [n for n in declared_functions(HEADERS[:1]) if not hasattr(L, n)]
     assert not missing, missing
+    from blackwell_tile_gemm_gb300 import probes
+    P = probes._L()
+    missing = [n for n in declared_functions(HEADERS[1:]) if not hasattr(P, n)]
+    assert not missing, missing
+    # the product library carries no probe entry point
+    assert not any(hasattr(L, n) for n in declared_functions(HEADERS[1:]))
 
 
 def test_status_strings_and_version(L):
