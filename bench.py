@@ -738,7 +738,8 @@ def run_configs(args):
                 # the same product through the 128 x 256 tile kernel, for comparison
                 ms_tile = median_ms(lambda: tg.gemm_bf16(A, B, D))
             else:
-                fn = lambda: tg.gemm_bf16(A, B, D, cta_pair=w.cta_pair, **epi)  # noqa: E731
+                fn = lambda: tg.gemm_bf16(A, B, D, cta_pair=w.cta_pair,  # noqa: E731
+                                          multicast=w.multicast, **epi)
         ms = median_ms(fn)
         ms_g = graph_ms(fn)
         code, _ = tg.tg_device_status()

@@ -117,7 +117,7 @@ def lib() -> ctypes.CDLL:
         L.tg_workspace_alloc_count.restype = ctypes.c_uint64
         L.tg_workspace_alloc_count.argtypes = []
         L.tg_gemm_repitch.restype = i32
-        L.tg_gemm_repitch.argtypes = [i64, i64, i64, i64, i64]
+        L.tg_gemm_repitch.argtypes = [i64, i64, i64, i64, i64, u32]
         L.tg_skinny_split_count.restype = i32
         L.tg_skinny_split_count.argtypes = [i64, i64, i32]
         for name in ("gemm_mxfp4_blockscaled", "gemm_nvfp4_blockscaled"):
@@ -403,9 +403,12 @@ def workspace_alloc_count() -> int:
     return int(lib().tg_workspace_alloc_count())
 
 
-def gemm_repitch(M: int, N: int, K: int, lda: int, ldb: int) -> int:
-    """Operands gemm_bf16 copies to a 128-byte row pitch first: bit 0 A, bit 1 B."""
-    r = lib().tg_gemm_repitch(int(M), int(N), int(K), int(lda), int(ldb))
+def gemm_repitch(M: int, N: int, K: int, lda: int, ldb: int, cta_pair: bool = False,
+                 multicast: bool = False) -> int:
+    """Operands gemm_bf16 copies to a 128-byte row pitch first (for operands in
+    the current device's memory): bit 0 A, bit 1 B."""
+    r = lib().tg_gemm_repitch(int(M), int(N), int(K), int(lda), int(ldb),
+                              _flags(cta_pair, multicast))
     if r < 0:
         raise TgError(-r, "tg_gemm_repitch")
     return r

@@ -343,7 +343,7 @@ int launch_gemm(int kind, const void* A, int64_t lda, const void* B, int64_t ldb
   int rc = TG_OK;
   if (kind == kKindBf16) {
     const bool mcast = bf16_uses_multicast(A, B, M, N, K, pair, mcast_flag);
-    const Bf16Repitch rp = bf16_repitch_plan(lda, ldb, M, N, K);
+    const Bf16Repitch rp = bf16_repitch_plan(lda, ldb, M, N, K, pair && mcast);
     if (rp.bytes != 0) {
       void* ws = device_workspace(rp.bytes, stream, &rc);
       if (ws == nullptr) return rc;
@@ -606,7 +606,10 @@ int64_t tg_workspace_bytes(int call, int64_t M, int64_t N, int64_t K, int64_t ld
   const bool pair = (flags & TG_FLAG_CTA_PAIR) != 0;
   switch (call) {
     case TG_CALL_GEMM_BF16:
-      return static_cast<int64_t>(bf16_repitch_plan(lda, ldb, M, N, K).bytes);
+      // Multicast pair clusters take no copy, but fall back to plain pairs
+      // (which may) for operands outside this device's memory: size for
+      // the plain kernel.
+      return static_cast<int64_t>(bf16_repitch_plan(lda, ldb, M, N, K, false).bytes);
     case TG_CALL_GEMM_MXFP8:
       if (K % 32) return -TG_ERR_INVALID_ARG;
       return static_cast<int64_t>(blockscaled_workspace_bytes(kKindMxf8, M, N, K, pair));
@@ -635,9 +638,12 @@ int tg_reserve_workspace(void* cuda_stream, int64_t bytes) {
 
 uint64_t tg_workspace_alloc_count(void) { return alloc_count(); }
 
-int tg_gemm_repitch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb) {
+int tg_gemm_repitch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, unsigned flags) {
   if (M < 0 || N < 0 || K < 0 || lda < 0 || ldb < 0) return -TG_ERR_INVALID_ARG;
-  const Bf16Repitch rp = bf16_repitch_plan(lda, ldb, M, N, K);
+  if (flags & ~static_cast<unsigned>(TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST))
+    return -TG_ERR_INVALID_ARG;
+  const bool pair_clusters = (flags & TG_FLAG_CTA_PAIR) && (flags & TG_FLAG_MULTICAST);
+  const Bf16Repitch rp = bf16_repitch_plan(lda, ldb, M, N, K, pair_clusters);
   return (rp.a ? 1 : 0) | (rp.b ? 2 : 0);
 }
 

@@ -109,7 +109,12 @@ int bf16_tail_split(int64_t M, int64_t N, int64_t K, bool pair, DeviceCtx* ctx) 
 // pitch costs ~4 bytes per element of HBM or L2 traffic; for 16-byte rows
 // it pays when the product is large against its operands, M*N/(M+N) >=
 // 1250.  For 32-byte rows the copy cost more than it saved (8192^2 x 1000,
-// 2016-byte rows: 108 -> 118 us).
+// 2016-byte rows: 108 -> 118 us).  Multicast clusters of two CTA pairs load
+// half as many B boxes, and there the copy no longer pays (graph replay,
+// 16-byte rows, with -> without the copy: 4000 x 3000 x 1000 26.8 -> 24.4
+// us, 6000^2 x 3000 136 -> 125 us, 8192^2 x 8000 at 8008-element rows 645
+// -> ~615 us; 8192^2 x 1000 107.1 -> 108.8 us), while plain pairs and
+// single CTAs still gain 10-15% from it at those shapes.
 
 namespace {
 
@@ -156,9 +161,10 @@ int row_alignment_class(int64_t ld) {
 
 }  // namespace
 
-Bf16Repitch bf16_repitch_plan(int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K) {
+Bf16Repitch bf16_repitch_plan(int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                              bool pair_clusters) {
   Bf16Repitch rp;
-  if (K < 128 || M <= 0 || N <= 0) return rp;
+  if (pair_clusters || K < 128 || M <= 0 || N <= 0) return rp;
   const double ratio = static_cast<double>(M) * static_cast<double>(N) / static_cast<double>(M + N);
   auto wants = [&](int64_t ld) { return row_alignment_class(ld) == 16 && ratio >= 1250.0; };
   rp.a = wants(lda);

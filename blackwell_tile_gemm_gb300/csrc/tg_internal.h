@@ -98,7 +98,10 @@ struct Bf16Repitch {
   int64_t kp = 0;
   size_t bytes = 0;  // workspace bytes; 0: no re-pitch
 };
-Bf16Repitch bf16_repitch_plan(int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K);
+// pair_clusters: the launch runs multicast clusters of two CTA pairs, which
+// take badly aligned rows as they are (no re-pitch).
+Bf16Repitch bf16_repitch_plan(int64_t lda, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                              bool pair_clusters);
 int launch_gemm_bf16_repitched(const Bf16Repitch& rp, const void* A, int64_t lda, const void* B,
                                int64_t ldb, void* D, int64_t ldd, int M, int N, int K,
                                int d_dtype, const Epi& epi, bool pair, bool mcast,

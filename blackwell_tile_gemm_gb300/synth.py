@@ -178,6 +178,7 @@ class Workload:
     epi_add: float     # epilogue constant (0: plain product)
     cta_pair: bool     # launch with cta_group::2 pairs
     describe: str
+    multicast: bool = False   # clusters of two MMA units sharing B by TMA multicast
 
     @property
     def flops(self) -> int:
@@ -193,8 +194,9 @@ WORKLOADS = {
                      "bf16 GEMM 8192^3, N(0,1)/sqrt(K) inputs, fp32 D, CTA pairs"),
     "mx8k": Workload("mx8k", "mxfp8", 8192, 8192, 8192, 4, "bf16", 0.0, True,
                      "MXFP8 GEMM 8192^3, E4M3 x E8M0/32 inputs, bf16 D"),
-    "ragged": Workload("ragged", "bf16", 4000, 3000, 1000, 5, "f32", 1.0, False,
-                       "bf16 GEMM 4000x3000x1000 + 1, U[-1,1) inputs, fp32 D"),
+    "ragged": Workload("ragged", "bf16", 4000, 3000, 1000, 5, "f32", 1.0, True,
+                       "bf16 GEMM 4000x3000x1000 + 1, U[-1,1) inputs, fp32 D, "
+                       "multicast clusters of two CTA pairs", multicast=True),
     "tr8k": Workload("tr8k", "transpose", 8192, 8192, 0, 6, "b16", 0.0, False,
                      "b16 transpose 8192x8192, random bit patterns"),
     "sk16_8k": Workload("sk16_8k", "skinny", 16, 8192, 8192, 9, "bf16", 0.0, False,

@@ -182,7 +182,10 @@ enum {
  * aligned) and the product is large against its operands (M*N/(M+N) >=
  * 1250), that operand is first copied into the stream's library workspace
  * at a 128-byte pitch (ceil(K/64)*64 elements per row; K elements read per
- * row); the result is the same, bit for bit.
+ * row); the result is the same, bit for bit.  Multicast clusters of CTA
+ * pairs (TG_FLAG_CTA_PAIR | TG_FLAG_MULTICAST over this device's memory)
+ * read such rows in place: with half as many B loads the copy no longer
+ * pays there.
  * Returns TG_OK once the kernel is enqueued, else an error (nothing enqueued).
  */
 int gemm_bf16(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
@@ -329,10 +332,12 @@ int tg_reserve_workspace(void* cuda_stream, int64_t bytes);
 uint64_t tg_workspace_alloc_count(void);
 
 /* tg_gemm_repitch -- which operands gemm_bf16 / gemm_bf16_ex re-pitch for
- * this shape and these row strides (see gemm_bf16): bit 0 A, bit 1 B (0:
- * neither); minus TG_ERR_INVALID_ARG for negative sizes.  Host arithmetic
- * only: no CUDA call, no device needed. */
-int tg_gemm_repitch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb);
+ * this shape, these row strides and these flags (see gemm_bf16), for
+ * operands in the current device's memory: bit 0 A, bit 1 B (0: neither);
+ * minus TG_ERR_INVALID_ARG for negative sizes or flags other than
+ * TG_FLAG_CTA_PAIR / TG_FLAG_MULTICAST.  Host arithmetic only: no CUDA call,
+ * no device needed. */
+int tg_gemm_repitch(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, unsigned flags);
 
 /* tg_skinny_split_count -- the number of K pieces gemm_bf16_skinny uses for
  * (N, K, split_k) on the current device, or minus a status code. */

@@ -198,10 +198,16 @@ def test_gather_rejects_before_launch(L):
 ])
 def test_repitch_rule(L, shape, lds, want):
     assert tg.gemm_repitch(*shape, *lds) == want
+    # the same for CTA pairs and for single-CTA multicast clusters
+    assert tg.gemm_repitch(*shape, *lds, cta_pair=True) == want
+    assert tg.gemm_repitch(*shape, *lds, multicast=True) == want
+    # multicast clusters of two CTA pairs read badly aligned rows in place
+    assert tg.gemm_repitch(*shape, *lds, cta_pair=True, multicast=True) == 0
 
 
-def test_repitch_rejects_negative_sizes(L):
-    assert L.tg_gemm_repitch(-1, 8, 8, 8, 8) == -tg.TG_ERR_INVALID_ARG
+def test_repitch_rejects_negative_sizes_and_unknown_flags(L):
+    assert L.tg_gemm_repitch(-1, 8, 8, 8, 8, 0) == -tg.TG_ERR_INVALID_ARG
+    assert L.tg_gemm_repitch(4000, 3000, 1000, 1000, 1000, 4) == -tg.TG_ERR_INVALID_ARG
 
 
 def test_multicast_query_falls_back_for_unknown_pointers(L):

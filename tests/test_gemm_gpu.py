@@ -147,21 +147,27 @@ def test_repeat_runs_are_bit_identical(tg):
     assert np.array_equal(d1, d2)
 
 
-def test_ragged_workload_full(tg, oracle):
-    # M=4000, N=3000, K=1000, D = A B^T + 1 in f32, every element.  Rows of
-    # 2000 bytes: both operands take the re-pitch copy first.
+@pytest.mark.parametrize("pair", [False, True, "mc"])
+def test_ragged_workload_full(tg, oracle, pair):
+    # M=4000, N=3000, K=1000, D = A B^T + 1 in f32, every element, in single
+    # CTAs (multicast clusters, chosen for this short K), CTA pairs and
+    # multicast clusters of two pairs (the workload's launch).  Rows of 2000
+    # bytes: both operands take the re-pitch copy first, except in the pair
+    # clusters, which read them in place.
     x = synth.make_inputs("ragged")
-    assert tg.gemm_repitch(4000, 3000, 1000, 1000, 1000) == 3
-    D = run_bf16(tg, x["A"], x["B"], "f32", add=1.0)
+    want = 0 if pair == "mc" else 3
+    assert tg.gemm_repitch(4000, 3000, 1000, 1000, 1000, cta_pair=bool(pair),
+                           multicast=pair == "mc") == want
+    D = run_bf16(tg, x["A"], x["B"], "f32", add=1.0, pair=pair)
     ref, mag = oracle.gemm_bf16(x["A"], x["B"], add=1.0)
-    assert_within(host_values(D), ref, mag, False, "ragged 4000x3000x1000")
+    assert_within(host_values(D), ref, mag, False, f"ragged 4000x3000x1000 ({pair})")
 
 
-@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("pair", [False, True, "mc"])
 def test_repitch_matches_aligned_strides_bit_for_bit(tg, pair):
-    # The same operands at lda = 1000 (re-pitched) and lda = 1024 (used in
-    # place) give the same bits: the copy changes where rows live, not the
-    # arithmetic.
+    # The same operands at lda = 1000 (re-pitched; pair clusters: read in
+    # place) and lda = 1024 (used in place) give the same bits: where rows
+    # live does not change the arithmetic.
     torch = torch_cuda()
     x = synth.make_inputs("ragged")
     M, N, K = 4000, 3000, 1000
@@ -172,8 +178,9 @@ def test_repitch_matches_aligned_strides_bit_for_bit(tg, pair):
     Bp[:, :K] = dev_bf16(x["B"])
     D1 = torch.full((M, N), float("nan"), device="cuda")
     D2 = torch.full((M, N), float("nan"), device="cuda")
-    tg.gemm_bf16(dev_bf16(x["A"]), dev_bf16(x["B"]), D1, epilogue_add=1.0, cta_pair=pair)
-    tg.gemm_bf16(Ap[:, :K], Bp[:, :K], D2, epilogue_add=1.0, cta_pair=pair)
+    kw = dict(cta_pair=bool(pair), multicast=pair == "mc")
+    tg.gemm_bf16(dev_bf16(x["A"]), dev_bf16(x["B"]), D1, epilogue_add=1.0, **kw)
+    tg.gemm_bf16(Ap[:, :K], Bp[:, :K], D2, epilogue_add=1.0, **kw)
     assert tg.tg_device_status()[0] == tg.TG_OK
     assert torch.equal(D1, D2)
 
