@@ -24,9 +24,10 @@ one line saying so and every rank exits 0.
 
 The line also carries what checks the timed work: the oracle's values on the
 CPU-baseline sample compared with the last timed step's outputs
-("parity"), the SM clock sampled while each kernel ran, and the fraction of
-the tensor pipe's own rate (SMs x FLOP per SM per clock from the rate probe x
-that clock).
+("parity"), the SM clock sampled while each kernel ran (NVML) and the one
+the GEMM kernels' own cycle counters saw (tg_kernel_clock_read), and the
+fraction of the tensor pipe's own rate (SMs x FLOP per SM per clock from the
+rate probe x a clock: the probe's own, and the kernel's).
 """
 from __future__ import annotations
 
@@ -398,6 +399,9 @@ def run_ours(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    # The GEMM kernels' own SM clock over the timed launches (their cycle
+    # counter against the global timer), beside NVML's samples.
+    tg.kernel_clock_record(True)
     with ClockSampler(gpu_ids(torch, 0), 0) as clk:
         time.sleep(0.005)                 # a few idle samples before the region
         h0 = time.perf_counter()          # the stream is idle: t_start runs at once
@@ -407,6 +411,9 @@ def run_ours(args):
         t_end.record(stream)
         torch.cuda.synchronize()
         time.sleep(0.002)
+    kclk = {"bf16": tg.kernel_clock_read(tg.TG_CLOCK_BF16),
+            "mxfp8": tg.kernel_clock_read(tg.TG_CLOCK_MXFP8)}
+    tg.kernel_clock_record(False)
     sms, probe = probe_rates(torch, dev)
     total_ms = t_start.elapsed_time(t_end)
     code, site = tg.tg_device_status()
@@ -435,6 +442,13 @@ def run_ours(args):
     def theoretical(tflops, kind):
         return tflops / probe[kind]["tflops"]
 
+    def at_kernel_clock(entry, tflops, kind):
+        # the pipe's peak at the clock the kernel itself ran at
+        mhz, units = kclk[kind]
+        if mhz > 0:
+            peak = sms * probe[kind]["flop_per_clk_per_sm"] * mhz * 1e6 / 1e12
+            entry.update(sm_mhz_in_kernel=mhz, frac_theoretical_at_kernel_clock=tflops / peak)
+
     kern = {}
     if run_bf16:
         t = flops_gemm / (bf16_ms * 1e-3) / 1e12
@@ -442,6 +456,7 @@ def run_ours(args):
         kern["gemm_bf16"] = {"ms": bf16_ms, "tflops": t, "frac_of_bf16_peak": t / peak_bf16,
                              "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"],
                              "frac_theoretical": theoretical(t, "bf16")}
+        at_kernel_clock(kern["gemm_bf16"], t, "bf16")
     if run_mx:
         t = flops_gemm / (mx_ms * 1e-3) / 1e12
         c = clk_by_kernel["gemm_mxfp8_blockscaled"]
@@ -449,6 +464,7 @@ def run_ours(args):
             "ms": mx_ms, "tflops": t, "frac_of_2x_bf16_peak": t / (2 * peak_bf16),
             "sm_mhz": c["sm_mhz"], "clock_samples": c["samples"],
             "frac_theoretical": theoretical(t, "mxfp8")}
+        at_kernel_clock(kern["gemm_mxfp8_blockscaled"], t, "mxfp8")
     if run_f4:
         t = flops_gemm / (mx_ms * 1e-3) / 1e12
         c = clk_by_kernel[names[1]]
@@ -487,13 +503,17 @@ def run_ours(args):
         roofline.update({
             "frac_theoretical": achieved / pr["tflops"],
             "theoretical_peak": pr["tflops"],
+            "frac_theoretical_at_kernel_clock": kern[dominant].get("frac_theoretical_at_kernel_clock"),
+            "kernel_sm_mhz": kern[dominant].get("sm_mhz_in_kernel"),
             "frac_theoretical_at_max_clock": achieved / at_max,
             "theoretical_basis": (
                 f"{sms} SMs x {pr['flop_per_clk_per_sm']:.0f} FLOP/clk/SM x {pr['mhz']:.0f} MHz: "
                 f"the rate probe's back-to-back tcgen05.mma on every SM, at the SM clock its "
                 f"cycle counter showed (NVML reports {max_mhz:.0f} MHz meanwhile; the SM cycle "
                 f"counter runs slower under tensor load); at {max_mhz:.0f} MHz the peak would "
-                f"be {at_max:.0f} TFLOP/s")})
+                f"be {at_max:.0f} TFLOP/s; frac_theoretical_at_kernel_clock takes the clock "
+                f"the kernel's own cycle counter showed over the timed launches "
+                f"(kernel_sm_mhz)")})
 
     # Check the timed work: the last step's outputs against the oracle on the
     # CPU-baseline sample (and the transpose against a host transpose).

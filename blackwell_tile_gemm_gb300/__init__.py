@@ -47,6 +47,10 @@ TG_CALL_GEMM_MXFP4 = 2
 TG_CALL_GEMM_NVFP4 = 3
 TG_CALL_GEMM_BF16_SKINNY = 4
 TG_CALL_GEMM_BF16_GATHER = 5
+TG_CLOCK_BF16 = 0
+TG_CLOCK_MXFP8 = 1
+TG_CLOCK_MXFP4 = 2
+TG_CLOCK_NVFP4 = 3
 
 _lock = threading.Lock()
 _lib = None
@@ -130,6 +134,11 @@ def lib() -> ctypes.CDLL:
         L.tile_transpose_b16.argtypes = [vp, i64, vp, i64, i64, i64, vp]
         L.tg_device_status.restype = i32
         L.tg_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.tg_kernel_clock_record.restype = i32
+        L.tg_kernel_clock_record.argtypes = [i32]
+        L.tg_kernel_clock_read.restype = i32
+        L.tg_kernel_clock_read.argtypes = [i32, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_uint64)]
         L.tg_set_wait_timeout_ns.restype = i32
         L.tg_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         L.tg_status_string.restype = ctypes.c_char_p
@@ -523,6 +532,22 @@ def tg_device_status(stream=None):
     site = ctypes.c_uint32(0)
     rc = lib().tg_device_status(_stream_handle(stream), ctypes.byref(site))
     return int(rc), int(site.value)
+
+
+def kernel_clock_record(enable: bool = True) -> None:
+    """Start (clearing the sums) or stop recording the SM clock of the GEMM
+    kernels on the current device; synchronises the device."""
+    _check(lib().tg_kernel_clock_record(1 if enable else 0), "tg_kernel_clock_record")
+
+
+def kernel_clock_read(kind: int):
+    """(average SM MHz, MMA units) of the recorded launches of `kind`
+    (TG_CLOCK_BF16, _MXFP8, _MXFP4, _NVFP4); synchronises the device."""
+    mhz = ctypes.c_double(0.0)
+    units = ctypes.c_uint64(0)
+    _check(lib().tg_kernel_clock_read(int(kind), ctypes.byref(mhz), ctypes.byref(units)),
+           "tg_kernel_clock_read")
+    return float(mhz.value), int(units.value)
 
 
 def tg_set_wait_timeout_ns(ns: int) -> None:

@@ -24,6 +24,10 @@ namespace tg {
 
 // Status record of each device: [0] code, [1] wait site, [2] block, [3] thread.
 __device__ uint32_t g_status_record[4];
+// SM clock readout of the GEMM kernels: per kind (dense bf16, MXFP8, MXFP4,
+// NVFP4), the SM cycles, nanoseconds and MMA units summed over the launches
+// made while tg_kernel_clock_record is on.
+__device__ unsigned long long g_kernel_clock[4][3];
 
 namespace {
 
@@ -94,8 +98,15 @@ DeviceCtx* current_ctx() {
     cuda_fail(e);
     return nullptr;
   }
+  void* clk = nullptr;
+  e = cudaGetSymbolAddress(&clk, g_kernel_clock);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return nullptr;
+  }
   c.num_sms = sms;
   c.status = static_cast<uint32_t*>(st);
+  c.clock_acc = static_cast<unsigned long long*>(clk);
   c.device = dev;
   return &c;
 }
@@ -704,6 +715,36 @@ int tg_device_status(void* cuda_stream, uint32_t* site) {
   // A launch that gave up may have left tail-split flags set: start over.
   if (rec[0] != TG_OK) reset_tail_flags();
   return static_cast<int>(rec[0]);
+}
+
+int tg_kernel_clock_record(int enable) {
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  ctx->clock_on.store(false);
+  // Launches already queued finish adding before the sums are read or cleared.
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (enable == 0) return TG_OK;
+  const unsigned long long zero[4][3] = {};
+  e = cudaMemcpyToSymbol(g_kernel_clock, zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e);
+  ctx->clock_on.store(true);
+  return TG_OK;
+}
+
+int tg_kernel_clock_read(int kind, double* mhz, uint64_t* units) {
+  if (kind < TG_CLOCK_BF16 || kind > TG_CLOCK_NVFP4 || mhz == nullptr)
+    return TG_ERR_INVALID_ARG;
+  DeviceCtx* ctx = current_ctx();
+  if (!ctx) return TG_ERR_CUDA;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned long long v[3] = {0, 0, 0};
+  e = cudaMemcpyFromSymbol(v, g_kernel_clock, sizeof(v), sizeof(v) * static_cast<size_t>(kind));
+  if (e != cudaSuccess) return cuda_fail(e);
+  *mhz = v[1] ? static_cast<double>(v[0]) * 1e3 / static_cast<double>(v[1]) : 0.0;
+  if (units) *units = v[2];
+  return TG_OK;
 }
 
 int tg_set_wait_timeout_ns(uint64_t ns) {

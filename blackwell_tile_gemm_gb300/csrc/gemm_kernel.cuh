@@ -97,6 +97,9 @@ struct GemmArgs {
   // Host side only (the kernel ignores it): the call must not allocate, so
   // the launcher never turns on the tail split, whose scratch is allocated.
   bool no_scratch;
+  // SM clock readout: when set, the MMA thread of each unit adds its SM
+  // cycles, nanoseconds and 1 to these three sums (tg_kernel_clock_record).
+  unsigned long long* clk;
 };
 
 // kKind_: kKindBf16 (dense bf16) or one of the block-scaled kinds kKindMxf8,
@@ -729,6 +732,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
+      const unsigned long long clk_c0 = clock64();
+      const uint64_t clk_g0 = global_timer_ns();
       const uint32_t acce0 = smem_addr(&acce_bar[0]);
       // K-major, 128-byte swizzled operands: 8-row groups 1024 bytes apart;
       // MMA k of a stage reads the 32-byte K slice k of each row.
@@ -806,6 +811,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           acc = 0;
           acc_phase ^= 1u;
         }
+      }
+      if (p.clk != nullptr) {
+        atomicAdd(p.clk, static_cast<unsigned long long>(clock64()) - clk_c0);
+        atomicAdd(p.clk + 1, static_cast<unsigned long long>(global_timer_ns() - clk_g0));
+        atomicAdd(p.clk + 2, 1ull);
       }
       if (!ok || *abort_flag) {
         // Gave up: wait until every MMA issued so far has finished with

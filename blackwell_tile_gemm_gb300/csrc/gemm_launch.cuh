@@ -100,6 +100,7 @@ int launch_gemm_cfg(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensor
   a.tail_items = 0;
   a.partials = nullptr;
   a.counters = nullptr;
+  a.clk = clock_slot(ctx, C::kKind);
   if (!args.no_scratch) {
     // Tail split: W full waves of whole tiles over all units; the R tiles of
     // a last, partial wave are cut into S K-pieces (S <= units / R, at most

@@ -1,6 +1,7 @@
 // Host-side pieces shared by the translation units of libtgemm.so.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -16,7 +17,17 @@ struct DeviceCtx {
   int device = -1;
   int num_sms = 0;
   uint32_t* status = nullptr;      // device address of the 4-word status record
+  // SM clock readout (tg_kernel_clock_record): device address of the
+  // [kind][cycles, nanoseconds, units] sums, and whether launches add to it.
+  unsigned long long* clock_acc = nullptr;
+  std::atomic<bool> clock_on{false};
 };
+
+// Accumulator slot of GEMM kind `kind` (gemm_kinds.h) for the next launch, or
+// nullptr while the clock readout is off.
+inline unsigned long long* clock_slot(DeviceCtx* ctx, int kind) {
+  return ctx->clock_on.load(std::memory_order_relaxed) ? ctx->clock_acc + 3 * kind : nullptr;
+}
 
 // Context of the current device (cudaGetDevice); nullptr on CUDA failure
 // (the failure is recorded for tg_last_cuda_error).

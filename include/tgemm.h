@@ -38,8 +38,9 @@
  *     A graph captured from a stream keeps that stream's workspace addresses:
  *     do not replay it concurrently with itself or with other work on it.
  *   - The only calls that synchronise are tg_device_status,
- *     tg_reserve_workspace and, without a reservation, a call that grows its
- *     stream's workspace.
+ *     tg_reserve_workspace, the SM clock readout (tg_kernel_clock_record /
+ *     _read) and, without a reservation, a call that grows its stream's
+ *     workspace.
  *   - Strides are in ELEMENTS and describe row-major 2-D arrays (unit inner
  *     stride).  Pointers are device pointers and must be 16-byte aligned;
  *     every row stride times the element size must be a multiple of 16 bytes.
@@ -432,6 +433,33 @@ int tile_transpose_b16(const void* in, int64_t ld_in, void* out, int64_t ld_out,
  * the device should be idle at that point.
  */
 int tg_device_status(void* cuda_stream, uint32_t* site);
+
+/*
+ * SM clock of the GEMM kernels.  NVML (nvidia-smi) can report the maximum SM
+ * clock while a power-capped tensor kernel actually runs several hundred MHz
+ * lower, and a kernel's fraction of the tensor pipe's peak depends on that
+ * clock.  While recording is on, every MMA unit (a CTA, or the leading CTA
+ * of a pair) of each gemm_* launch on the current device adds the SM cycles
+ * and nanoseconds (%clock64, %globaltimer) between the start and the end of
+ * its MMA issue into a sum kept per kind; the readout is their ratio.
+ *
+ * tg_kernel_clock_record -- enable != 0: clear the sums and record the
+ *   launches made after this call; 0: stop recording (the sums are kept).
+ *   Synchronises the device.  The skinny GEMM and the transpose do not record.
+ * tg_kernel_clock_read -- the average SM clock in MHz (0 if nothing was
+ *   recorded) of the launches of `kind` since recording was last enabled,
+ *   and the number of MMA units that contributed (`units` may be NULL).
+ *   Synchronises the device.  TG_ERR_INVALID_ARG for an unknown kind or a
+ *   NULL `mhz`.  Not on the pages: a measurement aid.
+ */
+enum {
+  TG_CLOCK_BF16 = 0,   /* gemm_bf16, gemm_bf16_ex, gemm_bf16_gather */
+  TG_CLOCK_MXFP8 = 1,  /* gemm_mxfp8_blockscaled(_ex, _noalloc)     */
+  TG_CLOCK_MXFP4 = 2,  /* gemm_mxfp4_blockscaled                    */
+  TG_CLOCK_NVFP4 = 3   /* gemm_nvfp4_blockscaled                    */
+};
+int tg_kernel_clock_record(int enable);
+int tg_kernel_clock_read(int kind, double* mhz, uint64_t* units);
 
 /* Deadline of every bounded pipeline wait, in nanoseconds (default 2e9).
  * Applies to launches made after the call; 0 is rejected. */
