@@ -446,6 +446,8 @@ int tg_device_status(void* cuda_stream, uint32_t* site);
  * tg_kernel_clock_record -- enable != 0: clear the sums and record the
  *   launches made after this call; 0: stop recording (the sums are kept).
  *   Synchronises the device.  The skinny GEMM and the transpose do not record.
+ *   A launch captured into a CUDA graph while recording is on keeps adding
+ *   whenever the graph is replayed, also after recording was stopped.
  * tg_kernel_clock_read -- the average SM clock in MHz (0 if nothing was
  *   recorded) of the launches of `kind` since recording was last enabled,
  *   and the number of MMA units that contributed (`units` may be NULL).
